@@ -1,0 +1,53 @@
+"""The pins catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a temporary copy of the oracle's C source (a
+dropped rescale term, a flipped sign, a wrong operand or index, a missing
+scale or log), builds it, and runs tests/test_oracle_pins.py against that
+copy in a subprocess.  The pin suite must fail for every mutant.  The
+committed oracle itself is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "fa_oracle.c")
+
+MUTANTS = {
+    "merge_drops_alpha": ("*l_out = alpha * l_a + beta * l_b;", "*l_out = l_a + beta * l_b;"),
+    "merge_u_wrong_factor": ("u_out[c] = alpha * u_a[c] + beta * u_b[c];",
+                             "u_out[c] = beta * u_a[c] + beta * u_b[c];"),
+    "softmax_sign_flipped": ("double p = exp(x[j] - m) / l;", "double p = exp(m - x[j]) / l;"),
+    "lse_missing_log": ("*lse_out = m + log(l);", "*lse_out = m + l;"),
+    "score_uses_values": ("acc += q[c] * widen_bf16(kbase[(size_t)j * d + c]);",
+                          "acc += q[c] * widen_bf16(vbase[(size_t)j * d + c]);"),
+    "scale_dropped": ("s[j] = scale * acc;", "s[j] = acc;"),
+    "causal_off_by_one": ("if (causal && i + 1 < nvalid) nvalid = i + 1;",
+                          "if (causal && i < nvalid) nvalid = i;"),
+    "key_len_ignored": ("if (key_len) nvalid = key_len[b] < nvalid ? key_len[b] : nvalid;", ""),
+    "online_correction_inverted": ("double corr = (j == 0) ? 0.0 : exp(m - m_new);",
+                                   "double corr = (j == 0) ? 0.0 : exp(m_new - m);"),
+    "reduce_weight_no_rescale": ("double w = l_k[k] * exp(m_k[k] - m_f) / l_f;",
+                                 "double w = l_k[k] / l_f;"),
+    "bf16_widen_wrong_half": ("uint32_t word = ((uint32_t)bits) << 16;",
+                              "uint32_t word = ((uint32_t)bits) << 15;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutant_c = tmp_path / f"{name}.c"
+    mutant_c.write_text(src.replace(old, new))
+    so = tmp_path / f"{name}.so"
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-fopenmp", str(mutant_c),
+                    "-o", str(so), "-lm"], check=True)
+    env = dict(os.environ, FA_ORACLE_LIB_OVERRIDE=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pin suite passed with mutant {name}:\n{r.stdout[-2000:]}"

@@ -1,0 +1,197 @@
+"""GB300-native exact tiled attention: Python binding of libfa.so.
+
+This module only marshals arguments: it checks that tensors are CUDA bf16 and
+contiguous, allocates outputs with torch, and passes raw device pointers and
+the current CUDA stream to the C ABI declared in ``include/fa.h``.  Every step
+of the computation runs in the library's CUDA kernels; there is no CPU or
+PyTorch fallback, and the calls raise if ``libfa.so`` is missing.
+
+    fa_forward(Q, K, V, causal=False, scale=None, key_len=None) -> (O, L)
+    fa_decode(q, Kcache, Vcache, seqlens, num_splits=0, ...)   -> (O, L)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = ["fa_forward", "fa_decode", "fa_decode_plan", "fa_decode_workspace_bytes",
+           "fa_device_error", "FaError", "library", "library_path", "STATUS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libfa.so")
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
+          4: "FA_ERR_WORKSPACE", 5: "FA_ERR_DEVICE_TIMEOUT"}
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def library():
+    """Load libfa.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(
+                f"{_LIB_PATH} is missing: build it with exact_attention_tiled_gb300.build.build()")
+        lib = ctypes.CDLL(_LIB_PATH)
+        lib.fa_forward.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp]
+        lib.fa_forward.restype = _i
+        lib.fa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float, _i,
+                                  _vp, ctypes.c_size_t, _vp]
+        lib.fa_decode.restype = _i
+        lib.fa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _vp]
+        lib.fa_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_decode_plan.argtypes = [_i, _i, _i, _i, _i, _vp, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]
+        lib.fa_decode_plan.restype = _i
+        lib.fa_status_string.argtypes = [_i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_device_error.argtypes = [_i, ctypes.POINTER(_i)]
+        lib.fa_device_error.restype = _i
+        lib.fa_version.restype = _i
+        _lib = lib
+        return lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _check_bf16(name, t, ndim):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA bfloat16 tensor")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _host_i32(x):
+    """(ctypes buffer, keep-alive) of a host int32 array, or (None, None)."""
+    if x is None:
+        return None, None
+    torch = _torch()
+    if isinstance(x, torch.Tensor):
+        vals = [int(v) for v in x.detach().cpu().tolist()]
+    else:
+        vals = [int(v) for v in x]
+    buf = (ctypes.c_int32 * len(vals))(*vals)
+    return ctypes.cast(buf, ctypes.c_void_p), buf
+
+
+def fa_forward(Q, K, V, causal=False, scale=None, key_len=None, out=None, lse=None,
+               return_lse=True, stream=None):
+    """Exact attention forward.  Q, K, V: CUDA bf16 [B, H, N, d]; returns (O, L).
+
+    key_len: optional CUDA int32 [B] key-padding lengths.  L is float32
+    [B, H, N] (None when return_lse=False and no `lse` buffer is given).
+    """
+    torch = _torch()
+    for n, t in (("Q", Q), ("K", K), ("V", V)):
+        _check_bf16(n, t, 4)
+    if K.shape != Q.shape or V.shape != Q.shape:
+        raise ValueError("Q, K, V must share the shape [B, H, N, d]")
+    B, H, N, d = Q.shape
+    if out is None:
+        out = torch.empty_like(Q)
+    else:
+        _check_bf16("out", out, 4)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), device=Q.device, dtype=torch.float32)
+    if key_len is not None:
+        if key_len.dtype != torch.int32 or not key_len.is_cuda or key_len.numel() != B:
+            raise TypeError("key_len must be a CUDA int32 tensor with B entries")
+        key_len = key_len.contiguous()
+    st = library().fa_forward(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), _ptr(lse), B, H, N, d,
+                              int(bool(causal)), float(scale) if scale is not None else 0.0,
+                              _ptr(key_len), _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, "fa_forward")
+    return out, lse
+
+
+def fa_decode_plan(B, H, Lmax, d, num_splits=0, seqlens_host=None, num_sms=0):
+    """(chunk_len, max_chunks) of the split plan fa_decode would use."""
+    hp, keep = _host_i32(seqlens_host)
+    c, m = _i(), _i()
+    st = library().fa_decode_plan(B, H, Lmax, d, num_splits, hp, num_sms, ctypes.byref(c), ctypes.byref(m))
+    del keep
+    if st != 0:
+        raise FaError(st, "fa_decode_plan")
+    return c.value, m.value
+
+
+def fa_decode_workspace_bytes(B, H, Lmax, d, num_splits=0, seqlens_host=None):
+    hp, keep = _host_i32(seqlens_host)
+    n = library().fa_decode_workspace_bytes(B, H, Lmax, d, num_splits, hp)
+    del keep
+    return int(n)
+
+
+def fa_decode(q, Kcache, Vcache, seqlens, num_splits=0, scale=None, seqlens_host=None,
+              out=None, lse=None, return_lse=True, workspace=None, stream=None):
+    """Split-KV single-query attention.  q: [B, H, d]; caches [B, H, Lmax, d].
+
+    seqlens: CUDA int32 [B].  seqlens_host: optional host copy used for the
+    split plan (defaults to a host copy of seqlens, which synchronises).
+    Returns (O [B, H, d] bf16, L [B, H] float32).
+    """
+    torch = _torch()
+    _check_bf16("q", q, 3)
+    _check_bf16("Kcache", Kcache, 4)
+    _check_bf16("Vcache", Vcache, 4)
+    B, H, Lmax, d = Kcache.shape
+    if Vcache.shape != Kcache.shape or tuple(q.shape) != (B, H, d):
+        raise ValueError("q must be [B, H, d] and the caches [B, H, Lmax, d]")
+    if seqlens.dtype != torch.int32 or not seqlens.is_cuda or seqlens.numel() != B:
+        raise TypeError("seqlens must be a CUDA int32 tensor with B entries")
+    seqlens = seqlens.contiguous()
+    if seqlens_host is None:
+        seqlens_host = seqlens.cpu()
+    hp, keep = _host_i32(seqlens_host)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    need = library().fa_decode_workspace_bytes(B, H, Lmax, d, num_splits, hp)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    st = library().fa_decode(_ptr(q), _ptr(Kcache), _ptr(Vcache), _ptr(seqlens), hp, _ptr(out),
+                             _ptr(lse), B, H, Lmax, d, float(scale) if scale is not None else 0.0,
+                             int(num_splits), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    del keep
+    if st != 0:
+        raise FaError(st, "fa_decode")
+    return out, lse
+
+
+def fa_device_error(clear=True):
+    """(status, site) of the device error word; synchronises the device."""
+    site = _i()
+    st = library().fa_device_error(int(bool(clear)), ctypes.byref(site))
+    return st, site.value

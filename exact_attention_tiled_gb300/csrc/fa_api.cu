@@ -1,0 +1,312 @@
+// fa_api.cu -- the C ABI of libfa.so: argument validation, split planning,
+// workspace layout and kernel launches.  Everything here runs on the host;
+// the arithmetic of the method lives in the kernels.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+// Device error word written by bounded waits (see fa_ptx.cuh).
+__device__ unsigned g_device_error = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+int g_decode_ctas[kMaxDevices][2] = {};
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+fa_status current_device(int *dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (*dev < 0 || *dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+// Address of the error word on the current device (looked up once per device).
+fa_status error_word(unsigned **out) {
+    int dev;
+    fa_status s = current_device(&dev);
+    if (s != FA_OK) return s;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return FA_ERR_CUDA;
+        g_err_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    *out = g_err_ptr[dev];
+    return FA_OK;
+}
+
+fa_status device_sm_count(int *out) {
+    int dev;
+    fa_status s = current_device(&dev);
+    if (s != FA_OK) return s;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return FA_ERR_CUDA;
+        g_sm_count[dev] = n;
+    }
+    *out = g_sm_count[dev];
+    return FA_OK;
+}
+
+fa_status device_decode_ctas(int d, int *out) {
+    int dev;
+    fa_status s = current_device(&dev);
+    if (s != FA_OK) return s;
+    const int idx = d == 128 ? 1 : 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_decode_ctas[dev][idx]) {
+        const int n = decode_ctas_per_sm(d);
+        if (n <= 0) return FA_ERR_CUDA;
+        g_decode_ctas[dev][idx] = n;
+    }
+    *out = g_decode_ctas[dev][idx];
+    return FA_OK;
+}
+
+int clamp_len(int v, int lmax) { return v < 0 ? 0 : (v > lmax ? lmax : v); }
+
+int round_up(long long v, int g) { return static_cast<int>((v + g - 1) / g * g); }
+
+// Split plan ("science-depth M4-055", trade-off 3: the chunk count is chosen
+// from the SM count and the sequence length; too many chunks make the
+// reduction dominate).  Pure host arithmetic.
+//
+//   fixed (num_splits > 0): every sequence gets num_splits chunks of
+//     ceil(len / num_splits) tokens rounded up to the granule; smax = num_splits.
+//   automatic, equal lengths: choose the per-sequence chunk count S that
+//     minimises waves(S) * (chunk(S) + overhead), waves counted against the
+//     resident CTA slots, so the work divides into whole waves.
+//   automatic, mixed lengths: one chunk length c for the batch that balances
+//     the per-chunk overhead against the tail of the last wave:
+//     c = sqrt(2 * overhead * total_tokens / slots); each sequence then gets
+//     ceil(len / c) chunks.
+constexpr int kOverheadTokens = 96;  // fixed cost of one CTA, in token-equivalents
+
+void plan_decode(int B, int H, int Lmax, int num_splits, const int32_t *seqlens_host, int slots,
+                 int *chunk_len, int *smax) {
+    long long total = 0;
+    int max_len = 0, min_len = Lmax;
+    for (int b = 0; b < B; ++b) {
+        const int len = seqlens_host ? clamp_len(seqlens_host[b], Lmax) : Lmax;
+        total += len;
+        max_len = len > max_len ? len : max_len;
+        min_len = len < min_len ? len : min_len;
+    }
+    total *= H;
+    if (max_len <= 0) {  // nothing to attend: one (empty) slot per (b, h)
+        *chunk_len = kDecodeGranule;
+        *smax = 1;
+        return;
+    }
+    if (num_splits > 0) {
+        int c = round_up((max_len + num_splits - 1) / num_splits, kDecodeGranule);
+        *chunk_len = c;
+        *smax = num_splits;
+        return;
+    }
+    if (slots < 1) slots = 1;
+    int c;
+    if (min_len == max_len) {
+        const long long units = static_cast<long long>(B) * H;
+        const int max_s = (max_len + kDecodeGranule - 1) / kDecodeGranule;
+        double best = 1e300;
+        c = round_up(max_len, kDecodeGranule);
+        for (int s = 1; s <= max_s && s <= 1024; ++s) {
+            const int cs = round_up((max_len + s - 1) / s, kDecodeGranule);
+            const int ns = (max_len + cs - 1) / cs;
+            const long long ctas = units * ns;
+            const long long waves = (ctas + slots - 1) / slots;
+            const double cost = static_cast<double>(waves) * (cs + kOverheadTokens);
+            if (cost < best - 1e-9) {
+                best = cost;
+                c = cs;
+            }
+        }
+    } else {
+        const double opt = std::sqrt(2.0 * kOverheadTokens * static_cast<double>(total) / slots);
+        c = round_up(static_cast<long long>(opt), kDecodeGranule);
+        if (c < 4 * kDecodeGranule) c = 4 * kDecodeGranule;
+        const int cmax = round_up(max_len, kDecodeGranule);
+        if (c > cmax) c = cmax;
+    }
+    *chunk_len = c;
+    *smax = (max_len + c - 1) / c;
+}
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+size_t workspace_for(int B, int H, int smax, int d) {
+    const size_t slots = static_cast<size_t>(B) * H * smax;
+    return align256(slots * d * sizeof(float)) + align256(slots * 2 * sizeof(float));
+}
+
+bool decode_shape_ok(int B, int H, int Lmax, int d) {
+    return B >= 1 && H >= 1 && Lmax >= 1 && B <= 65535 && H <= 65535 && (d == 64 || d == 128);
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char *fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+        case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+    }
+    return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_device_error(int clear, int *site) {
+    unsigned *ptr = nullptr;
+    fa_status s = error_word(&ptr);
+    if (s != FA_OK) return s;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, ptr, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+    if (clear) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(ptr, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    if (site) *site = static_cast<int>(v & 0x7FFFFFFFu);
+    return v ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}
+
+fa_status fa_decode_plan(int B, int H, int Lmax, int d, int num_splits, const int32_t *seqlens_host,
+                         int num_sms, int *chunk_len, int *max_chunks) {
+    if (!chunk_len || !max_chunks || !decode_shape_ok(B, H, Lmax, d)) return FA_ERR_INVALID_ARG;
+    int slots = 1;
+    if (num_splits > 0) {
+        // a fixed chunk count needs no device information
+    } else if (num_sms > 0) {
+        slots = num_sms * 2;
+    } else {
+        int sms = 0, per = 0;
+        fa_status s = device_sm_count(&sms);
+        if (s != FA_OK) return s;
+        s = device_decode_ctas(d, &per);
+        if (s != FA_OK) return s;
+        slots = sms * per;
+    }
+    plan_decode(B, H, Lmax, num_splits, seqlens_host, slots, chunk_len, max_chunks);
+    return FA_OK;
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int Lmax, int d, int num_splits,
+                                 const int32_t *seqlens_host) {
+    if (!decode_shape_ok(B, H, Lmax, d)) return 0;
+    int chunk = 0, smax = 0;
+    if (num_splits > 0) {
+        smax = num_splits;
+    } else if (fa_decode_plan(B, H, Lmax, d, num_splits, seqlens_host, 0, &chunk, &smax) != FA_OK) {
+        return 0;
+    }
+    return workspace_for(B, H, smax, d);
+}
+
+fa_status fa_decode(const void *q, const void *Kcache, const void *Vcache, const int32_t *seqlens,
+                    const int32_t *seqlens_host, void *O, float *L, int B, int H, int Lmax, int d,
+                    float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                    fa_stream_t stream) {
+    if (!q || !Kcache || !Vcache || !seqlens || !O) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || Lmax < 1 || B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(Kcache, 16) || !aligned(Vcache, 16) || !aligned(O, 16) ||
+        !aligned(seqlens, 4) || (L && !aligned(L, 4)))
+        return FA_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale))) return FA_ERR_INVALID_ARG;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(d));
+
+    int chunk = 0, smax = 0;
+    fa_status s = fa_decode_plan(B, H, Lmax, d, num_splits, seqlens_host, 0, &chunk, &smax);
+    if (s != FA_OK) return s;
+    if (smax < 1 || smax > 65535 * 32) return FA_ERR_UNSUPPORTED;
+    const size_t need = workspace_for(B, H, smax, d);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return FA_ERR_WORKSPACE;
+
+    unsigned *err = nullptr;
+    s = error_word(&err);
+    if (s != FA_OK) return s;
+
+    DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    const size_t slots = static_cast<size_t>(B) * H * smax;
+    p.q = q;
+    p.K = Kcache;
+    p.V = Vcache;
+    p.seqlens = seqlens;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                          align256(slots * d * sizeof(float)));
+    p.O = O;
+    p.L = L;
+    p.B = B;
+    p.H = H;
+    p.Lmax = Lmax;
+    p.num_splits = num_splits > 0 ? num_splits : 0;
+    p.chunk_len = chunk;
+    p.smax = smax;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+    if (launch_decode(p, d, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *L, int B, int H,
+                     int N, int d, int causal, float scale, const int32_t *key_len,
+                     fa_stream_t stream) {
+    if (!Q || !K || !V || !O) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
+        (L && !aligned(L, 4)) || (key_len && !aligned(key_len, 4)))
+        return FA_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H * N > (1ll << 40)) return FA_ERR_UNSUPPORTED;
+    if (!(std::isfinite(scale))) return FA_ERR_INVALID_ARG;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(d));
+
+    unsigned *err = nullptr;
+    fa_status s = error_word(&err);
+    if (s != FA_OK) return s;
+
+    PrefillParams p;
+    std::memset(&p, 0, sizeof p);
+    p.Q = Q;
+    p.K = K;
+    p.V = V;
+    p.O = O;
+    p.L = L;
+    p.key_len = key_len;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.causal = causal;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+    if (launch_prefill(p, d, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// fa_internal.h -- launch interfaces between the C ABI layer (fa_api.cu) and
+// the kernel translation units.  Host-side only; no torch types anywhere.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// ------------------------------------------------------------------ decode
+struct DecodeParams {
+    const void *q;          // bf16 [B, H, d]
+    const void *K;          // bf16 [B, H, Lmax, d]
+    const void *V;          // bf16 [B, H, Lmax, d]
+    const int32_t *seqlens; // device [B]
+    float *part_o;          // fp32 [B, H, smax, d]   O_k = u_k / l_k
+    float *part_ml;         // fp32 [B, H, smax, 2]   (m_k, l_k), natural-log units
+    void *O;                // bf16 [B, H, d]
+    float *L;               // fp32 [B, H] or nullptr
+    int B, H, Lmax;
+    int num_splits;         // > 0: fixed chunk count per sequence
+    int chunk_len;          // tokens per chunk when num_splits <= 0 (multiple of 64)
+    int smax;               // partial slots per (b, h)
+    float scale_log2;       // scale * log2(e)
+    unsigned *err;          // device error word
+};
+
+constexpr int kDecodeTile = 64;      // tokens per staged tile
+constexpr int kDecodeGranule = 64;   // chunk lengths are multiples of this
+
+// Launch the split kernel and the merge kernel on `stream`.
+cudaError_t launch_decode(const DecodeParams &p, int d, cudaStream_t stream);
+// Resident split-kernel CTAs per SM for head dimension d (0 on error).
+int decode_ctas_per_sm(int d);
+
+// ------------------------------------------------------------------ prefill
+struct PrefillParams {
+    const void *Q, *K, *V;  // bf16 [B, H, N, d]
+    void *O;                // bf16 [B, H, N, d]
+    float *L;               // fp32 [B, H, N] or nullptr
+    const int32_t *key_len; // device [B] or nullptr
+    int B, H, N;
+    int causal;
+    float scale_log2;       // scale * log2(e)
+    unsigned *err;
+};
+
+cudaError_t launch_prefill(const PrefillParams &p, int d, cudaStream_t stream);
+
+}  // namespace fa

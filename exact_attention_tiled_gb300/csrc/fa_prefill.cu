@@ -1,0 +1,516 @@
+// fa_prefill.cu -- exact attention forward on sm_103a tensor cores.
+//
+// What is computed ("Infra: Flash Attention", Algorithm 1 "FlashAttention
+// forward", in the FlashAttention-2 order: query tiles outside, KV tiles
+// inside, normalisation delayed to the end):
+//
+//   for each query tile Q_i:  m = -inf, l = 0, U = 0
+//     for each KV tile j:     S = Q_i K_j^T * scale           (tensor cores)
+//                             mask S (rows with no valid key skip the update)
+//                             m' = max(m, rowmax S), alpha = exp(m - m')
+//                             W = exp(S - m'), l = alpha l + rowsum W
+//                             U = alpha U + W V_j              (tensor cores)
+//                             m = m'
+//     O_i = U / l,  L_i = m + log l
+//
+// Causal masking skips KV tiles wholly in the future and masks the diagonal
+// tile on chip (same page, the causal figure; CMU 10-423 Lecture 18, 4.3).
+//
+// How it maps onto one GB300 SM (the FlashAttention-4 arrangement described
+// on the same page, section "FlashAttention-4": two query tiles per CTA so
+// the tensor core works on one tile's GEMM while the other tile's softmax
+// runs):
+//   * warp 8, one lane: TMA producer.  Loads Q for both query tiles once,
+//     then streams K_0, V_0, K_1, V_1, ... through a ring of shared-memory
+//     slots (128-byte swizzled, 64-column boxes).
+//   * warp 9: allocates tensor memory; one lane issues every tcgen05.mma:
+//       S_t = Q_t K_j^T        (A, B from shared memory, fp32 into TMEM)
+//       O_t += P_t V_j         (A = P from TMEM, B = V from shared memory)
+//     and signals completion through tcgen05.commit -> mbarrier.
+//   * warps 0-3 / 4-7: softmax warpgroups for query tile 0 / 1, one thread
+//     per query row.  They read S from TMEM, mask, update (m, l), write
+//     P = bf16(exp2(S*scale*log2e - m)) over the first half of S's TMEM
+//     columns, and rescale O in TMEM by alpha when some row's max moved.
+//     At the end they normalise O by 1/l and write O and L.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 after it.
+//
+// The MMA issue order per KV step is PV_0(j), S_0(j+1), PV_1(j), S_1(j+1):
+// S_t(j+1) overwrites the P_t(j) that PV_t(j) reads, which relies on the
+// tensor core executing one CTA's MMAs in issue order; and the barrier that
+// announces S_t(j+1) also covers PV_t(j), so the softmax may rescale O_t
+// as soon as it sees S_t(j+1).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BM = 128;          // query rows per tile (MMA M)
+constexpr int BN = 128;          // keys per KV tile (MMA N of Q K^T, K of P V)
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+enum {
+    kSiteQ = 0x201, kSiteKvFull = 0x202, kSiteKvEmpty = 0x203, kSiteP = 0x204, kSiteS = 0x205,
+    kSiteO = 0x206, kSiteDrain = 0x207, kSiteMmaDone = 0x208
+};
+
+template <int D>
+struct Cfg {
+    static constexpr int kColBlocks = D / 64;                 // 128-byte swizzle atoms per row
+    static constexpr int kTileBytes = BM * D * 2;             // one 128-row bf16 tile
+    static constexpr int kSlots = (D == 128) ? 4 : 8;         // KV ring slots (K and V alternate)
+    static constexpr int kQOff = 0;
+    static constexpr int kRingOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
+    // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_ready[2], o_final[2], mma_done
+    static constexpr int kNumBars = 1 + 2 * kSlots + 7;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;    // tmem base + abort flag
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // +1024 for base alignment
+};
+
+struct TmapSet {
+    CUtensorMap q, k, v;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, unsigned *err, int site,
+                                              volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            report_timeout(err, site);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ TmapSet tm, const PrefillParams p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte swizzled tiles need 1024-byte aligned bases.
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t q_smem = sbase + C::kQOff;
+    const uint32_t ring = sbase + C::kRingOff;
+    const uint32_t bars = sbase + C::kBarOff;
+    const uint32_t bar_q = bars;
+    auto bar_kv_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto bar_kv_empty = [&](int s) { return bars + 8u * (1 + C::kSlots + s); };
+    auto bar_s_full = [&](int t) { return bars + 8u * (1 + 2 * C::kSlots + t); };
+    auto bar_p_ready = [&](int t) { return bars + 8u * (3 + 2 * C::kSlots + t); };
+    auto bar_o_final = [&](int t) { return bars + 8u * (5 + 2 * C::kSlots + t); };
+    const uint32_t bar_mma_done = bars + 8u * (7 + 2 * C::kSlots);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int npairs = gridDim.x;
+    const int pair = npairs - 1 - static_cast<int>(blockIdx.x);  // heaviest causal pairs first
+    const int bh = b * p.H + h;
+    const int N = p.N;
+
+    // ---- per-CTA work bounds (identical in every thread)
+    int klen = N;
+    if (p.key_len) {
+        const int v = p.key_len[b];
+        klen = v < 0 ? 0 : (v > N ? N : v);
+    }
+    int row0[2], nkv[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        row0[t] = pair * 2 * BM + t * BM;
+        if (row0[t] >= N) {
+            nkv[t] = 0;
+            continue;
+        }
+        int kend = klen;
+        if (p.causal) {
+            const int qend = min(N, row0[t] + BM);
+            kend = min(kend, qend);
+        }
+        nkv[t] = (kend + BN - 1) / BN;
+    }
+    const int ntot = max(nkv[0], nkv[1]);
+
+    // ---- set-up: barriers, TMEM
+    if (threadIdx.x == 0) {
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < C::kSlots; ++s) {
+            mbar_init(bar_kv_full(s), 1);
+            mbar_init(bar_kv_empty(s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar_s_full(t), 1);
+            mbar_init(bar_p_ready(t), 4);
+            mbar_init(bar_o_final(t), 1);
+        }
+        mbar_init(bar_mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        // ================================================= TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm.q);
+            prefetch_tmap(&tm.k);
+            prefetch_tmap(&tm.v);
+            const uint64_t pol_q = l2_policy_evict_first();
+            const uint64_t pol_kv = l2_policy_evict_normal();
+            mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int cb = 0; cb < C::kColBlocks; ++cb)
+                    tma_load_3d(q_smem + t * C::kTileBytes + cb * (BM * 128), &tm.q, cb * 64, row0[t], bh,
+                                bar_q, pol_q);
+            int issued = 0;
+            for (int j = 0; j < ntot && !*abort_flag; ++j) {
+                for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
+                    const int item = 2 * j + kv;
+                    const int s = item % C::kSlots;
+                    if (item >= C::kSlots &&
+                        !wait_or_abort(bar_kv_empty(s), ((item / C::kSlots) - 1) & 1, p.err, kSiteKvEmpty,
+                                       abort_flag))
+                        break;
+                    mbar_arrive_expect_tx(bar_kv_full(s), C::kTileBytes);
+                    const CUtensorMap *map = kv ? &tm.v : &tm.k;
+#pragma unroll
+                    for (int cb = 0; cb < C::kColBlocks; ++cb)
+                        tma_load_3d(ring + s * C::kTileBytes + cb * (BN * 128), map, cb * 64, j * BN, bh,
+                                    bar_kv_full(s), pol_kv);
+                    ++issued;
+                }
+            }
+            // Drain: no copy may still be in flight when the CTA exits.
+            mbar_wait(bar_q, 0, p.err, kSiteDrain);
+            const int first = issued > C::kSlots ? issued - C::kSlots : 0;
+            for (int item = first; item < issued; ++item)
+                mbar_wait(bar_kv_full(item % C::kSlots), (item / C::kSlots) & 1, p.err, kSiteDrain);
+        }
+    } else if (warp == kMmaWarp) {
+        // ================================================= MMA issuer
+        if (lane == 0 && ntot > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);
+            auto issue_s = [&](int t, uint32_t kslot) {
+                const uint32_t qa = q_smem + t * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+                    mma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024),
+                           sdesc_sw128(kslot + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, uint32_t vslot, int j) {
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
+                           sdesc_sw128(vslot + kk * 2048, BN * 128, 1024), idesc_o,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = wait_or_abort(bar_q, 0, p.err, kSiteQ, abort_flag);
+            // prologue: S_t(0)
+            if (ok) ok = wait_or_abort(bar_kv_full(0), 0, p.err, kSiteKvFull, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                for (int t = 0; t < 2; ++t)
+                    if (nkv[t] > 0) {
+                        issue_s(t, ring);
+                        mma_commit(bar_s_full(t));
+                    }
+                mma_commit(bar_kv_empty(0));
+            }
+            for (int j = 0; ok && j < ntot; ++j) {
+                const int iv = 2 * j + 1, ik = 2 * j + 2;
+                const int sv = iv % C::kSlots, sk = ik % C::kSlots;
+                const uint32_t vslot = ring + sv * C::kTileBytes;
+                const uint32_t kslot = ring + sk * C::kTileBytes;
+                const bool more = (j + 1 < ntot);
+                ok = wait_or_abort(bar_kv_full(sv), (iv / C::kSlots) & 1, p.err, kSiteKvFull, abort_flag);
+                bool k_ready = false;
+                for (int t = 0; ok && t < 2; ++t) {
+                    if (j < nkv[t]) {
+                        ok = wait_or_abort(bar_p_ready(t), j & 1, p.err, kSiteP, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(t, vslot, j);
+                        if (j + 1 == nkv[t]) mma_commit(bar_o_final(t));
+                    }
+                    if (t == 1) mma_commit(bar_kv_empty(sv));
+                    if (j + 1 < nkv[t]) {
+                        if (!k_ready) {
+                            ok = wait_or_abort(bar_kv_full(sk), (ik / C::kSlots) & 1, p.err, kSiteKvFull,
+                                               abort_flag);
+                            if (!ok) break;
+                            tc_fence_after();
+                            k_ready = true;
+                        }
+                        issue_s(t, kslot);
+                        mma_commit(bar_s_full(t));
+                    }
+                }
+                if (ok && more) {
+                    if (!k_ready) {
+                        // no tile needed K_{j+1}: still consume the slot
+                        ok = wait_or_abort(bar_kv_full(sk), (ik / C::kSlots) & 1, p.err, kSiteKvFull,
+                                           abort_flag);
+                    }
+                    mma_commit(bar_kv_empty(sk));
+                }
+            }
+        }
+        if (lane == 0 && ntot > 0) {
+            // every MMA issued above has completed before TMEM is released
+            mma_commit(bar_mma_done);
+            mbar_wait(bar_mma_done, 0, p.err, kSiteMmaDone);
+        }
+        __syncwarp();
+    } else {
+        // ================================================= softmax warpgroups
+        const int t = warp >> 2;              // query tile of this warpgroup
+        const int quarter = warp & 3;         // TMEM lane quarter
+        const int r = quarter * 32 + lane;    // row within the tile
+        const int qi = row0[t] + r;           // query index
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t s_addr = tmem + lane_off + t * 128;
+        const uint32_t o_addr = tmem + lane_off + 256 + t * D;
+        const float sl2 = p.scale_log2;
+
+        float m_run = -INFINITY;  // running max, log2 units of the scaled score
+        float l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv[t]; ++j) {
+            ok = wait_or_abort(bar_s_full(t), j & 1, p.err, kSiteS, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            __syncwarp();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+
+            // mask: keys beyond key_len / the sequence, and the causal future
+            const int kbase = j * BN;
+            const bool need_mask = (kbase + BN > klen) || (p.causal && kbase + BN > row0[t]);
+            if (need_mask) {
+                int lim = klen - kbase;
+                if (p.causal) lim = min(lim, qi - kbase + 1);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
+            }
+            // row max with independent partial maxima
+            float mx[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sr[c][e]));
+#pragma unroll
+            for (int a = 1; a < 8; ++a) mx[0] = fmaxf(mx[0], mx[a]);
+            const float m_new = fmaxf(m_run, mx[0] * sl2);
+            // a row that has seen no valid key yet keeps a finite base so no
+            // -inf - (-inf) appears; its weights are then all zero
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = ex2(m_run - m_use);  // 0 when m_run = -inf
+            const float nm = -m_use;
+
+            float ls[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) ls[a] = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float w0 = ex2(fmaf(__uint_as_float(sr[c][e]), sl2, nm));
+                    const float w1 = ex2(fmaf(__uint_as_float(sr[c][e + 1]), sl2, nm));
+                    ls[e & 7] += w0;
+                    ls[(e + 1) & 7] += w1;
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(w0, w1);
+                    pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&pr);
+                }
+                // P columns 16c .. 16c+15 of this tile's S region
+#pragma unroll
+                for (int e = 0; e < 16; ++e) sr[c][e] = pk[e];
+            }
+            {
+                uint32_t lo[32], hi[32];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    lo[e] = sr[0][e];
+                    lo[16 + e] = sr[1][e];
+                    hi[e] = sr[2][e];
+                    hi[16 + e] = sr[3][e];
+                }
+                tmem_st32(s_addr + 0, lo);
+                tmem_st32(s_addr + 32, hi);
+            }
+            float rs = 0.f;
+#pragma unroll
+            for (int a = 0; a < 8; ++a) rs += ls[a];
+            l_run = l_run * alpha + rs;
+            m_run = m_new;
+
+            // correction: U <- alpha U (O holds PV(j-1) complete at this point)
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; c += 2) {
+                    uint32_t o0[32], o1[32];
+                    tmem_ld32(o_addr + c * 32, o0);
+                    tmem_ld32(o_addr + (c + 1) * 32, o1);
+                    tmem_wait_ld();
+                    reg_fence(o0);
+                    reg_fence(o1);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        o0[e] = __float_as_uint(__uint_as_float(o0[e]) * alpha);
+                        o1[e] = __float_as_uint(__uint_as_float(o1[e]) * alpha);
+                    }
+                    tmem_st32(o_addr + c * 32, o0);
+                    tmem_st32(o_addr + (c + 1) * 32, o1);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_p_ready(t));
+        }
+
+        // ---- epilogue: O = U / l, L = m + log l
+        const bool have = ok && nkv[t] > 0;
+        if (have) ok = wait_or_abort(bar_o_final(t), 0, p.err, kSiteO, abort_flag);
+        const bool store = qi < N && row0[t] < N;
+        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.O) + (static_cast<size_t>(bh) * N + qi) * D;
+        if (have && ok) {
+            tc_fence_after();
+            __syncwarp();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(o_addr + c * 32, o);
+                tmem_wait_ld();
+                reg_fence(o);
+                if (store) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __nv_bfloat162 pr = __floats2bfloat162_rn(
+                                __uint_as_float(o[v * 8 + 2 * e]) * inv, __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
+                            w[e] = *reinterpret_cast<const uint32_t *>(&pr);
+                        }
+                        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+            if (store && p.L)
+                p.L[static_cast<size_t>(bh) * N + qi] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+        } else if (!have && store) {
+            // no valid key for this row (key_len = 0): O = 0, L = -inf
+            uint4 *dst = reinterpret_cast<uint4 *>(orow);
+            for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+            if (p.L) p.L[static_cast<size_t>(bh) * N + qi] = -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 3-D view [B*H][N][d] of a bf16 tensor; box = 64 columns x 128 rows x 1.
+bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
+    TmapSet tm;
+    std::memset(&tm, 0, sizeof tm);
+    const int BH = p.B * p.H;
+    if (!make_map(&tm.q, p.Q, BH, p.N, D) || !make_map(&tm.k, p.K, BH, p.N, D) ||
+        !make_map(&tm.v, p.V, BH, p.N, D))
+        return cudaErrorInvalidValue;
+    const int smem = Cfg<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int npairs = (p.N + 2 * BM - 1) / (2 * BM);
+    dim3 grid(npairs, p.H, p.B);
+    prefill_kernel<D><<<grid, kThreads, smem, stream>>>(tm, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams &p, int d, cudaStream_t stream) {
+    return d == 128 ? launch_d<128>(p, stream) : launch_d<64>(p, stream);
+}
+
+}  // namespace fa

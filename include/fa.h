@@ -1,0 +1,161 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library (libfa.so).
+ *
+ * Two operations, both defined by the pages this library follows:
+ *
+ *   fa_forward  exact scaled-dot-product attention O = softmax(Q K^T * scale) V,
+ *               computed tile by tile with the online-softmax state (m, l, U)
+ *               so that the N x N scores S and weights P never reach global
+ *               memory; it also returns the per-row log-sum-exp
+ *               L = m + log l = log sum_j exp(S_ij).
+ *               ("Infra: Flash Attention", sections "Attention and its scope",
+ *               "Tiled computation and the forward pass" with Algorithm 1
+ *               "FlashAttention forward", and "Backward and recomputation"
+ *               for L.)
+ *
+ *   fa_decode   Flash-Decoding: one query per (batch, head) over a long KV
+ *               cache.  The cache is split into chunks; one kernel writes a
+ *               partial state (m_k, l_k, O_k) per chunk and a second kernel
+ *               merges them with the log-sum-exp reduction
+ *               m = max_k m_k, l = sum_k l_k exp(m_k - m),
+ *               O = sum_k O_k l_k exp(m_k - m) / l.
+ *               ("science-depth M4-055: Flash-Decoding", "Flash-Decoding
+ *               Algorithm" steps 1-3 and trade-off 3 on the chunk count.)
+ *
+ * Conventions shared by every entry point
+ *   - Tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never frees or retains them.  bf16 = IEEE bfloat16 (2 bytes).
+ *   - Layouts are dense row-major with the last dimension contiguous.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and performs no host synchronisation.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     rejected call launches nothing and returns FA_ERR_INVALID_ARG or
+ *     FA_ERR_UNSUPPORTED.  A failed CUDA launch returns FA_ERR_CUDA.
+ *   - Device pointers must be 16-byte aligned (tensor-memory-accelerator
+ *     copies require it).
+ *   - Kernels bound every wait on a barrier.  A wait that runs out sets a
+ *     device-side error word and the kernel returns early; the outputs of
+ *     that call are then undefined.  fa_device_error() reports it.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad size or flag */
+    FA_ERR_UNSUPPORTED = 2,     /* valid request this build does not handle (e.g. d not 64/128) */
+    FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed */
+    FA_ERR_WORKSPACE = 4,       /* workspace missing or smaller than required */
+    FA_ERR_DEVICE_TIMEOUT = 5   /* a bounded in-kernel wait ran out (see fa_device_error) */
+} fa_status;
+
+typedef void *fa_stream_t; /* cudaStream_t */
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+/*
+ * fa_forward -- exact attention forward, one pass over Q tiles.
+ *
+ *   Q, K, V  bf16 [B, H, N, d], contiguous.
+ *   O        bf16 [B, H, N, d] output: O_i = sum_j P_ij V_j, rounded to
+ *            nearest-even bf16 from fp32.
+ *   L        float [B, H, N] output, natural-log LSE of the scaled scores,
+ *            or NULL to skip it.  A query row with no valid key gets O = 0
+ *            and L = -inf (the pages leave that case to the operator).
+ *   B, H, N  batch, heads, sequence length (queries and keys); all >= 1,
+ *            B * H <= 65535 * 65535.
+ *   d        head dimension, 64 or 128 (others: FA_ERR_UNSUPPORTED).
+ *   causal   0: every query sees every key; 1: query i sees keys j <= i
+ *            (upper-left aligned, square).  Key tiles wholly in the future
+ *            are skipped, diagonal tiles are masked on chip.
+ *   scale    score multiplier; <= 0 selects 1/sqrt(d).
+ *   key_len  NULL, or a DEVICE int32 [B]: keys j >= key_len[b] of batch b
+ *            are masked (right key padding).  Values are clamped to
+ *            [0, N]; key_len[b] = 0 leaves every row of b without keys.
+ *   stream   cudaStream_t.
+ *
+ * Arithmetic: bf16 inputs, fp32 tensor-core accumulation of Q K^T and of
+ * W V, fp32 softmax state; P is rounded to bf16 before the W V product.
+ */
+FA_API fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *L,
+                     int B, int H, int N, int d, int causal, float scale,
+                     const int32_t *key_len, fa_stream_t stream);
+
+/*
+ * fa_decode -- split-KV single-query attention (Flash-Decoding).
+ *
+ *   q             bf16 [B, H, d]: one query per (b, h).
+ *   Kcache,Vcache bf16 [B, H, Lmax, d]; row t of (b, h) holds token t.
+ *   seqlens       DEVICE int32 [B]: tokens 0 .. seqlens[b]-1 are attended;
+ *                 values are clamped to [0, Lmax].
+ *   seqlens_host  HOST copy of seqlens used to plan the split without a
+ *                 device synchronisation, or NULL (then every sequence is
+ *                 planned as if it were Lmax long; results are identical).
+ *   O             bf16 [B, H, d] output.  L: float [B, H] natural-log LSE or
+ *                 NULL.  A sequence of length 0 gets O = 0, L = -inf.
+ *   d             64 or 128.  scale <= 0 selects 1/sqrt(d).
+ *   num_splits    > 0: every sequence is cut into num_splits chunks of
+ *                 ceil(len / num_splits) tokens rounded up to a multiple of
+ *                 64 (so a short sequence may use fewer chunks);
+ *                 <= 0: automatic, one chunk length for the whole batch
+ *                 chosen from the SM count and the sequence lengths, which
+ *                 gives each sequence its own chunk count.
+ *   workspace     device scratch of at least fa_decode_workspace_bytes(...)
+ *                 bytes, 256-byte aligned; holds the per-chunk partials.
+ *                 Not read before it is written; may be reused across calls
+ *                 that are ordered on the GPU.
+ */
+FA_API fa_status fa_decode(const void *q, const void *Kcache, const void *Vcache,
+                    const int32_t *seqlens, const int32_t *seqlens_host,
+                    void *O, float *L,
+                    int B, int H, int Lmax, int d, float scale, int num_splits,
+                    void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * Workspace bytes fa_decode needs for these arguments (same meaning as
+ * there; seqlens_host may be NULL).  Returns 0 for arguments fa_decode
+ * would reject.
+ */
+FA_API size_t fa_decode_workspace_bytes(int B, int H, int Lmax, int d, int num_splits,
+                                 const int32_t *seqlens_host);
+
+/*
+ * The split plan fa_decode would use: writes the chunk length in tokens and
+ * the largest per-sequence chunk count.  num_sms <= 0 asks the current
+ * device; a positive value plans for that many SMs (host-only, no CUDA
+ * call).  Returns FA_OK or FA_ERR_INVALID_ARG.
+ */
+FA_API fa_status fa_decode_plan(int B, int H, int Lmax, int d, int num_splits,
+                         const int32_t *seqlens_host, int num_sms,
+                         int *chunk_len, int *max_chunks);
+
+/* Human-readable name of a status code (static string). */
+FA_API const char *fa_status_string(fa_status s);
+
+/*
+ * Device-side error word of the current device: 0 when no bounded wait has
+ * run out since the last clear, otherwise FA_ERR_DEVICE_TIMEOUT with the
+ * wait site in *site (may be NULL).  Synchronises the device.  clear != 0
+ * resets the word.
+ */
+FA_API fa_status fa_device_error(int clear, int *site);
+
+/* Library ABI version (major * 100 + minor). */
+FA_API int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

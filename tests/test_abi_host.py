@@ -1,0 +1,157 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library loads without a GPU, exports every entry point include/fa.h
+declares, rejects bad arguments before touching CUDA, and plans decode splits
+with pure host arithmetic.
+"""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_tiled_gb300 import build
+    build.build()
+    import exact_attention_tiled_gb300 as fa
+    return fa.library()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    return sorted(set(re.findall(r"FA_API\s+[\w\s\*]*?\b(fa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = _declared_symbols()
+    assert {"fa_forward", "fa_decode", "fa_decode_workspace_bytes", "fa_decode_plan",
+            "fa_status_string", "fa_device_error", "fa_version"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_symbols():
+        assert hasattr(lib, name), f"libfa.so does not export {name}"
+
+
+def test_status_strings(lib):
+    for code, name in [(0, b"FA_OK"), (1, b"FA_ERR_INVALID_ARG"), (2, b"FA_ERR_UNSUPPORTED"),
+                       (3, b"FA_ERR_CUDA"), (4, b"FA_ERR_WORKSPACE"), (5, b"FA_ERR_DEVICE_TIMEOUT")]:
+        assert lib.fa_status_string(code) == name
+    assert lib.fa_version() >= 100
+
+
+FAKE = 0x100000  # a 16-byte aligned, never-dereferenced address
+
+
+def _fwd(lib, **kw):
+    a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, L=None, B=1, H=1, N=16, d=64, causal=0, scale=0.0,
+             key_len=None)
+    a.update(kw)
+    return lib.fa_forward(a["Q"], a["K"], a["V"], a["O"], a["L"], a["B"], a["H"], a["N"], a["d"],
+                          a["causal"], ctypes.c_float(a["scale"]), a["key_len"], None)
+
+
+def test_forward_rejects_bad_arguments_before_cuda(lib):
+    assert _fwd(lib, Q=None) == 1
+    assert _fwd(lib, O=None) == 1
+    assert _fwd(lib, N=0) == 1
+    assert _fwd(lib, B=0) == 1
+    assert _fwd(lib, H=-3) == 1
+    assert _fwd(lib, causal=2) == 1
+    assert _fwd(lib, K=FAKE + 8) == 1          # not 16-byte aligned
+    assert _fwd(lib, L=FAKE + 2) == 1          # not 4-byte aligned
+    assert _fwd(lib, key_len=FAKE + 1) == 1
+    assert _fwd(lib, scale=float("nan")) == 1
+    assert _fwd(lib, d=96) == 2
+    assert _fwd(lib, d=256) == 2
+    assert _fwd(lib, B=70000) == 1
+
+
+def _dec(lib, **kw):
+    a = dict(q=FAKE, K=FAKE, V=FAKE, sl=FAKE, slh=None, O=FAKE, L=None, B=2, H=2, Lmax=128, d=128,
+             scale=0.0, splits=4, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    return lib.fa_decode(a["q"], a["K"], a["V"], a["sl"], a["slh"], a["O"], a["L"], a["B"], a["H"],
+                         a["Lmax"], a["d"], ctypes.c_float(a["scale"]), a["splits"], a["ws"], a["wsb"],
+                         None)
+
+
+def test_decode_rejects_bad_arguments_before_cuda(lib):
+    assert _dec(lib, q=None) == 1
+    assert _dec(lib, sl=None) == 1
+    assert _dec(lib, Lmax=0) == 1
+    assert _dec(lib, V=FAKE + 4) == 1
+    assert _dec(lib, d=80) == 2
+    # fixed splits: the workspace check needs no device
+    assert _dec(lib, ws=None) == 4
+    assert _dec(lib, wsb=16) == 4
+    assert _dec(lib, ws=FAKE + 16) == 4        # workspace must be 256-byte aligned
+
+
+def test_workspace_bytes_fixed_splits(lib):
+    B, H, Lmax, d, S = 3, 5, 1000, 128, 7
+    got = lib.fa_decode_workspace_bytes(B, H, Lmax, d, S, None)
+    slots = B * H * S
+    up = lambda v: (v + 255) // 256 * 256
+    assert got == up(slots * d * 4) + up(slots * 2 * 4)
+    assert lib.fa_decode_workspace_bytes(B, H, Lmax, 96, S, None) == 0
+    assert lib.fa_decode_workspace_bytes(0, H, Lmax, d, S, None) == 0
+
+
+def _plan(B, H, Lmax, d, splits, seqlens=None, sms=152):
+    import exact_attention_tiled_gb300 as fa
+    return fa.fa_decode_plan(B, H, Lmax, d, splits, seqlens, sms)
+
+
+def test_plan_fixed_splits():
+    for splits in (1, 8, 32, 128):
+        c, m = _plan(1, 32, 32768, 128, splits)
+        assert m == splits
+        assert c % 64 == 0 and c * splits >= 32768 and c == -(-(32768 // splits) // 64) * 64
+    # short sequence with many splits: chunks are at least one granule
+    c, m = _plan(1, 1, 100, 128, 128, [100])
+    assert c == 64 and m == 128
+
+
+def test_plan_auto_uniform_fills_whole_waves():
+    slots = 152 * 2
+    c, m = _plan(1, 32, 32768, 128, 0)
+    assert c % 64 == 0 and m * c >= 32768
+    ctas = 32 * m
+    waves = math.ceil(ctas / slots)
+    # the chosen split leaves at most ~10% of the last wave idle
+    assert ctas / (waves * slots) > 0.9, (c, m, ctas)
+    # one sequence per SM slot or more: a single chunk
+    c, m = _plan(64, 32, 2048, 128, 0)
+    assert m == 1 and c == 2048
+
+
+def test_plan_auto_mixed_lengths():
+    import torch
+    g = torch.Generator().manual_seed(5)
+    lens = torch.randint(1024, 65537, (16,), generator=g, dtype=torch.int32).tolist()
+    c, m = _plan(16, 32, 65536, 128, 0, lens)
+    assert c % 64 == 0 and 256 <= c <= 65536
+    assert m == math.ceil(max(lens) / c)
+    total_ctas = sum(32 * math.ceil(L / c) for L in lens)
+    assert total_ctas >= 4 * 152 * 2   # several waves, so the tail is short
+
+
+def test_plan_empty_and_clamped():
+    c, m = _plan(2, 2, 500, 64, 0, [0, 0])
+    assert m == 1
+    c2, m2 = _plan(2, 2, 500, 64, 0, [10_000, -5])   # clamped to [0, Lmax]
+    assert m2 * c2 >= 500
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import exact_attention_tiled_gb300 as fa
+    monkeypatch.setattr(fa, "_lib", None)
+    monkeypatch.setattr(fa, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        fa.library()

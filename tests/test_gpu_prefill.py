@@ -1,0 +1,106 @@
+"""Parity of the tcgen05 prefill path (through the C ABI) with the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_tiled_gb300 import workloads
+from gpu_util import compare
+
+pytestmark = pytest.mark.gpu
+
+
+def fa():
+    import exact_attention_tiled_gb300 as m
+    m.library()
+    return m
+
+
+def _fwd(Q, K, V, causal, key_len=None):
+    dev = torch.device("cuda")
+    kl = None if key_len is None else torch.as_tensor(key_len, dtype=torch.int32).to(dev)
+    O, L = fa().fa_forward(Q.to(dev), K.to(dev), V.to(dev), causal=causal, key_len=kl)
+    torch.cuda.synchronize()
+    return O.float().cpu().numpy(), L.cpu().numpy()
+
+
+def test_tiny_workload_full():
+    """B1 H1 N256 d64, non-causal, seed 0: every element against the oracle."""
+    inp = workloads.make("tiny_n256_d64")
+    O, L = _fwd(inp["Q"], inp["K"], inp["V"], False)
+    Oref, Lref = oracle.sdpa_forward(inp["Q"], inp["K"], inp["V"], causal=False)
+    compare("tiny", O, L, Oref, Lref)
+
+
+CASES = [
+    # B, H, N, d, causal, key_len
+    (2, 3, 1000, 128, True, None),
+    (2, 2, 777, 64, False, None),
+    (1, 2, 1, 64, False, None),
+    (1, 1, 127, 128, True, None),
+    (1, 2, 129, 64, True, None),
+    (1, 1, 256, 128, False, None),
+    (1, 1, 640, 64, True, None),
+    (2, 2, 300, 128, False, [1, 300]),
+    (2, 2, 300, 64, True, [150, 7]),
+    (3, 1, 384, 128, False, [0, 384, 200]),
+    (2, 1, 513, 128, True, [513, 1]),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,key_len", CASES)
+def test_small_ragged_full(B, H, N, d, causal, key_len):
+    Q, K, V = workloads.prefill_inputs(B, H, N, d, seed=N + d + B)
+    O, L = _fwd(Q, K, V, causal, key_len)
+    Oref, Lref = oracle.sdpa_forward(Q, K, V, causal=causal, key_len=key_len)
+    compare(f"B{B} H{H} N{N} d{d} c{int(causal)} kl{key_len}", O, L, Oref, Lref)
+
+
+def test_causal_first_row_is_first_value():
+    Q, K, V = workloads.prefill_inputs(1, 4, 512, 128, seed=3)
+    O, _ = _fwd(Q, K, V, True)
+    np.testing.assert_array_equal(O[:, :, 0], V[:, :, 0].float().numpy())
+
+
+def test_single_valid_key_returns_that_value():
+    Q, K, V = workloads.prefill_inputs(2, 2, 300, 64, seed=4)
+    O, _ = _fwd(Q, K, V, False, [1, 1])
+    for i in (0, 77, 299):
+        np.testing.assert_array_equal(O[:, :, i], V[:, :, 0].float().numpy())
+
+
+def _sampled(name, nrows, seed, use_key_len=True):
+    inp = workloads.make(name)
+    Q, K, V, causal = inp["Q"], inp["K"], inp["V"], inp["causal"]
+    kl = inp.get("key_len") if use_key_len else None
+    O, L = _fwd(Q, K, V, causal, kl)
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
+    B, H, N, d = Q.shape
+    rows = workloads.sample_indices(B * H * N, nrows, seed).numpy()
+    # include tile boundaries of the first head
+    rows = np.unique(np.concatenate([rows, [127, 128, 255, 256, N - 128, N - 1]]))
+    Oref, Lref = oracle.sdpa_rows(Q, K, V, rows, causal=causal, key_len=kl)
+    compare(name, O.reshape(-1, d)[rows], L.reshape(-1)[rows], Oref, Lref)
+
+
+@pytest.mark.slow
+def test_batched_d64_sampled():
+    """B8 H16 N2048 d64 (x0.5), non-causal, no padding; 2048 sampled rows."""
+    _sampled("prefill_b8h16_n2048_d64", 2048, 31, use_key_len=False)
+
+
+@pytest.mark.slow
+def test_batched_d64_key_padding_sampled():
+    """Same workload with per-batch key lengths U[N/2, N]."""
+    _sampled("prefill_b8h16_n2048_d64", 2048, 32)
+
+
+@pytest.mark.slow
+def test_causal_8k_d128_sampled():
+    """B1 H32 N8192 d128 causal; 1024 sampled rows."""
+    _sampled("prefill_causal_b1h32_n8192_d128", 1024, 33)
+
+
+def test_prefill_no_device_error_recorded():
+    st, site = fa().fa_device_error(clear=True)
+    assert st == 0, f"bounded wait ran out at site {site:#x}"

@@ -1,0 +1,448 @@
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one pass of the forward kernel over the 8k causal prefill workload
+(B1 H32 N8192 d128, bf16, seed 2), the headline of the metric (TFLOP/s of
+algorithmic work: only unmasked score entries count).  The split-KV decode
+over a 32768-token cache (B1 H32 d128, seed 4, automatic chunking) is timed
+the same way each step and reported under "decode" (GB/s of K and V read).
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream; the L2 cache is flushed (a 256 MiB write) between
+steps, outside the events.  Clocks are sampled with nvidia-smi during the
+timed region.  `--impl reference` times the float64 CPU oracle instead, on a
+bounded sample of the same workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+(N > 1 is launched by torchrun: one independent replica per GPU, weak scaling.)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOP/s vs BF16 TC peak; split-KV decode HBM GB/s vs peak"
+PREFILL = "prefill_causal_b1h32_n8192_d128"
+DECODE = "decode_b1h32_l32768_d128"
+FLUSH_BYTES = 256 << 20
+
+
+def prefill_flops(B, H, N, d, causal):
+    """Algorithmic FLOPs: 2*d for Q.K and 2*d for W.V per unmasked score."""
+    pairs = N * (N + 1) // 2 if causal else N * N
+    return 4.0 * d * pairs * B * H
+
+
+def decode_bytes(H, lens, d):
+    """Algorithmic bytes: every cached K and V row of every (b, h) read once."""
+    return float(sum(2 * H * n * d * 2 for n in lens))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_tiled_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(kernel)
+    if not ent or ent.get("sources_sha") != kernel_sources_hash():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.strip().split(",") for r in f if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import exact_attention_tiled_gb300 as fa
+    from exact_attention_tiled_gb300 import workloads
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = fa.library()
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+
+    # ---- inputs resident in HBM
+    wp = workloads.WORKLOADS[PREFILL]
+    Q, K, V = workloads.prefill_inputs(wp.B, wp.H, wp.N, wp.d, wp.seed, device=dev)
+    O = torch.empty_like(Q)
+    L = torch.empty((wp.B, wp.H, wp.N), device=dev, dtype=torch.float32)
+    wd = workloads.WORKLOADS[DECODE]
+    q, Kc, Vc = workloads.decode_inputs(wd.B, wd.H, wd.N, wd.d, wd.seed, device=dev)
+    seqlens = workloads.decode_seqlens(wd.B, wd.N, wd.seed)
+    seq_dev = seqlens.to(dev)
+    Od = torch.empty_like(q)
+    Ld = torch.empty((wd.B, wd.H), device=dev, dtype=torch.float32)
+    ws = torch.empty(fa.fa_decode_workspace_bytes(wd.B, wd.H, wd.N, wd.d, 0, seqlens), device=dev,
+                     dtype=torch.uint8)
+    chunk, nchunk = fa.fa_decode_plan(wd.B, wd.H, wd.N, wd.d, 0, seqlens)
+    flush = torch.empty(FLUSH_BYTES, device=dev, dtype=torch.uint8)
+
+    def prefill():
+        fa.fa_forward(Q, K, V, causal=True, out=O, lse=L)
+
+    def decode():
+        fa.fa_decode(q, Kc, Vc, seq_dev, num_splits=0, seqlens_host=seqlens, out=Od, lse=Ld,
+                     workspace=ws)
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        prefill()
+        decode()
+    torch.cuda.synchronize()
+    st, site = fa.fa_device_error(clear=True)
+    if st != 0:
+        raise RuntimeError(f"device error word set during warm-up (site {site:#x})")
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    pf_ms, dc_ms = [], []
+    launches = 0
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t_wall = time.perf_counter()
+        for _ in range(args.steps):
+            flush.fill_(1)
+            a, b = ev(), ev()
+            a.record(stream)
+            prefill()
+            b.record(stream)
+            launches += 1
+            flush.fill_(2)
+            c, d = ev(), ev()
+            c.record(stream)
+            decode()
+            d.record(stream)
+            launches += 2
+            torch.cuda.synchronize()
+            pf_ms.append(a.elapsed_time(b))
+            dc_ms.append(c.elapsed_time(d))
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.summary()
+    st, site = fa.fa_device_error(clear=True)
+    if st != 0:
+        raise RuntimeError(f"device error word set during timing (site {site:#x})")
+
+    # ---- chunk-count sweep of the decode path (same inputs, L2 flushed each time)
+    sweep = {}
+    for splits in tuple(wd.splits) + (0,):
+        ws_s = torch.empty(fa.fa_decode_workspace_bytes(wd.B, wd.H, wd.N, wd.d, splits, seqlens),
+                           device=dev, dtype=torch.uint8)
+        ts = []
+        for i in range(3 + 5):
+            flush.fill_(4)
+            a, b = ev(), ev()
+            a.record(stream)
+            fa.fa_decode(q, Kc, Vc, seq_dev, num_splits=splits, seqlens_host=seqlens, out=Od, lse=Ld,
+                         workspace=ws_s)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b))
+        sweep["auto" if splits == 0 else str(splits)] = round(
+            decode_bytes(wd.H, seqlens.tolist(), wd.d) / (statistics.mean(ts) * 1e-3) / 1e9, 1)
+
+    # ---- end to end through the public call with host buffers
+    Qh, Kh, Vh = (t.cpu().pin_memory() for t in (Q, K, V))
+    Oh = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    Lh = torch.empty(L.shape, dtype=L.dtype).pin_memory()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(3)
+        a, b = ev(), ev()
+        a.record(stream)
+        Qd = Qh.to(dev, non_blocking=True)
+        Kd = Kh.to(dev, non_blocking=True)
+        Vd = Vh.to(dev, non_blocking=True)
+        Od_, Ld_ = fa.fa_forward(Qd, Kd, Vd, causal=True)
+        Oh.copy_(Od_, non_blocking=True)
+        Lh.copy_(Ld_, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    h2d = 3 * Q.numel() * Q.element_size()
+    d2h = O.numel() * O.element_size() + L.numel() * L.element_size()
+
+    flops = prefill_flops(wp.B, wp.H, wp.N, wp.d, wp.causal)
+    dbytes = decode_bytes(wd.H, seqlens.tolist(), wd.d)
+    pf = statistics.mean(pf_ms)
+    dc = statistics.mean(dc_ms)
+    ee = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([pf, dc, ee], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        pf, dc, ee = t.tolist()
+
+    tflops = world * flops / (pf * 1e-3) / 1e12
+    gbs = world * dbytes / (dc * 1e-3) / 1e9
+    e2e_tflops = world * flops / (ee * 1e-3) / 1e12
+    per_gpu_tflops = flops / (pf * 1e-3) / 1e12
+    per_gpu_gbs = dbytes / (dc * 1e-3) / 1e9
+    src = peaks["source"]
+    result = {
+        "metric": METRIC,
+        "value": round(tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(pf, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": PREFILL, "B": wp.B, "H": wp.H, "N": wp.N, "d": wp.d, "causal": True,
+                   "seed": wp.seed, "flops_per_step": flops, "parallelism": "replicas",
+                   "l2": "flushed between steps (256 MiB write outside the timed events)"},
+        "roofline": {"bound": "tensor", "achieved": round(per_gpu_tflops, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(per_gpu_tflops / peaks["bf16_tflops"], 4),
+                     "peak_source": f"bf16 burst, of {src}",
+                     "traffic": recorded_traffic("prefill_kernel"),
+                     "kernel": "prefill_kernel<128>"},
+        "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(ee, 4),
+                "path": "pinned host Q,K,V -> device, fa_forward, O and L -> pinned host"},
+        "decode": {"workload": DECODE, "value": round(gbs, 1), "unit": "GB/s",
+                   "ms_per_step": round(dc, 4), "bytes_per_step": dbytes, "num_splits": "auto",
+                   "chunk_len": chunk, "chunks_per_seq": nchunk, "gbs_by_num_splits": sweep,
+                   "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1),
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": round(per_gpu_gbs / peaks["hbm_gbs"], 4),
+                                "frac_of_8tbs_nominal": round(per_gpu_gbs / 8000.0, 4),
+                                "peak_source": f"HBM copy, of {src}",
+                                "traffic": recorded_traffic("decode_split_kernel"),
+                                "kernel": "decode_split_kernel<128> + decode_merge_kernel<128>"}},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    return result
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_sample(seconds_target, seed=0):
+    """Time the float64 oracle on sampled rows of the prefill workload.
+
+    Returns (TFLOP/s of algorithmic work, threads, description)."""
+    import numpy as np
+    import oracle
+    from exact_attention_tiled_gb300 import workloads
+
+    wp = workloads.WORKLOADS[PREFILL]
+    Q, K, V = workloads.prefill_inputs(wp.B, wp.H, wp.N, wp.d, wp.seed)
+    threads = oracle.max_threads()
+    total = wp.B * wp.H * wp.N
+    rng = np.random.default_rng(seed)
+
+    def run(nrows):
+        rows = np.sort(rng.choice(total, size=nrows, replace=False))
+        i = rows % wp.N
+        work = float(np.sum(4.0 * wp.d * (i + 1)))
+        t0 = time.perf_counter()
+        oracle.sdpa_rows(Q, K, V, rows, causal=True, nthreads=threads)
+        return work, time.perf_counter() - t0
+
+    w, t = run(max(64, threads * 8))
+    rate = w / max(t, 1e-6)
+    nrows = int(min(total, max(64, seconds_target * rate / (4.0 * wp.d * wp.N / 2))))
+    w, t = run(nrows)
+    return w / t / 1e12, threads, f"{nrows} random query rows of {PREFILL} ({w:.3e} FLOP in {t:.1f} s)"
+
+
+def run_reference(args):
+    per_step = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    vals = []
+    desc = ""
+    threads = 0
+    for i in range(args.warmup + args.steps):
+        v, threads, desc = oracle_sample(per_step, seed=i)
+        if i >= args.warmup:
+            vals.append(v)
+    val = statistics.mean(vals)
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": val,
+        "unit": "TFLOP/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": None,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": PREFILL, "B": 1, "H": 32, "N": 8192, "d": 128, "causal": True, "seed": 2},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: {desc}"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_profile_case(args):
+    """Warm-up launches plus `steps` launches of one kernel, nothing else (for ncu)."""
+    import torch
+    import exact_attention_tiled_gb300 as fa
+    from exact_attention_tiled_gb300 import workloads
+    dev = torch.device("cuda", 0)
+    if args.profile == "prefill":
+        wp = workloads.WORKLOADS[PREFILL]
+        Q, K, V = workloads.prefill_inputs(wp.B, wp.H, wp.N, wp.d, wp.seed, device=dev)
+        run = lambda: fa.fa_forward(Q, K, V, causal=True)
+    else:
+        wd = workloads.WORKLOADS[DECODE]
+        q, Kc, Vc = workloads.decode_inputs(wd.B, wd.H, wd.N, wd.d, wd.seed, device=dev)
+        seqlens = workloads.decode_seqlens(wd.B, wd.N, wd.seed)
+        sd = seqlens.to(dev)
+        run = lambda: fa.fa_decode(q, Kc, Vc, sd, num_splits=0, seqlens_host=seqlens)
+    for _ in range(args.warmup + args.steps):
+        run()
+    torch.cuda.synchronize()
+    st, site = fa.fa_device_error(clear=True)
+    print(json.dumps({"profile_case": args.profile, "launches": args.warmup + args.steps,
+                      "device_error": st}))
+    if st != 0:
+        sys.exit(1)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+                    help="only launch one kernel warmup+steps times (for ncu captures)")
+    args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args)
+        return
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        v, threads, desc = oracle_sample(args.cpu_seconds)
+        res["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                               "sample": desc}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -214,13 +214,16 @@ __global__ void __launch_bounds__(kSplitThreads) decode_split_kernel(const Decod
 #pragma unroll
                 for (int it = 0; it < ITERS; ++it) {
                     const int tok = warp * 16 + it * TPI + sub;
-                    const float pw = ex2(sc[it] - m_new);  // 0 for masked tokens
-                    st.l += pw;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(vs + tok * kRowBytes + cl * 16);
-                    float vf[8];
-                    bf16x8_to_f32(raw, vf);
+                    // rows past the chunk end hold stale shared memory: never read them
+                    if (tok < valid) {
+                        const float pw = ex2(sc[it] - m_new);
+                        st.l += pw;
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(vs + tok * kRowBytes + cl * 16);
+                        float vf[8];
+                        bf16x8_to_f32(raw, vf);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) st.o[e] = fmaf(pw, vf[e], st.o[e]);
+                        for (int e = 0; e < 8; ++e) st.o[e] = fmaf(pw, vf[e], st.o[e]);
+                    }
                 }
                 st.m = m_new;
             }

@@ -58,6 +58,7 @@ constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleLog2 = 8.0f;  // move the exponent base only when the max grows by > 2^8
 
 enum {
     kSiteQ = 0x201, kSiteKvFull = 0x202, kSiteKvEmpty = 0x203, kSiteP = 0x204, kSiteS = 0x205,
@@ -255,7 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool more = (j + 1 < ntot);
                 ok = wait_or_abort(bar_kv_full(sv), (iv / C::kSlots) & 1, p.err, kSiteKvFull, abort_flag);
                 bool k_ready = false;
-                for (int t = 0; ok && t < 2; ++t) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (!ok) break;
                     if (j < nkv[t]) {
                         ok = wait_or_abort(bar_p_ready(t), j & 1, p.err, kSiteP, abort_flag);
                         if (!ok) break;
@@ -297,16 +300,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = warp >> 2;              // query tile of this warpgroup
         const int quarter = warp & 3;         // TMEM lane quarter
         const int r = quarter * 32 + lane;    // row within the tile
-        const int qi = row0[t] + r;           // query index
+        const int my_row0 = t ? row0[1] : row0[0];
+        const int my_nkv = t ? nkv[1] : nkv[0];
+        const int qi = my_row0 + r;           // query index
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + t * 128;
         const uint32_t o_addr = tmem + lane_off + 256 + t * D;
         const float sl2 = p.scale_log2;
 
-        float m_run = -INFINITY;  // running max, log2 units of the scaled score
+        // Conditional rescaling ("Infra: Flash Attention", "Conditional
+        // rescaling invariant"): l and U are kept relative to a base r that
+        // only moves when the row max exceeds r + kRescaleLog2; u(r)/l(r) does
+        // not depend on r, and with r within kRescaleLog2 of the max every
+        // weight stays <= 2^kRescaleLog2.  r is in log2 units of the scaled score.
+        float r_base = -INFINITY;
         float l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < nkv[t]; ++j) {
+        for (int j = 0; j < my_nkv; ++j) {
             ok = wait_or_abort(bar_s_full(t), j & 1, p.err, kSiteS, abort_flag);
             if (!ok) break;
             tc_fence_after();
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // mask: keys beyond key_len / the sequence, and the causal future
             const int kbase = j * BN;
-            const bool need_mask = (kbase + BN > klen) || (p.causal && kbase + BN > row0[t]);
+            const bool need_mask = (kbase + BN > klen) || (p.causal && kbase + BN > my_row0);
             if (need_mask) {
                 int lim = klen - kbase;
                 if (p.causal) lim = min(lim, qi - kbase + 1);
@@ -330,36 +340,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 32; ++e)
                         if (c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
             }
-            // row max with independent partial maxima
-            float mx[8];
-#pragma unroll
-            for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
+            // row max: four independent chains of three-input maxima
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sr[c][e]));
-#pragma unroll
-            for (int a = 1; a < 8; ++a) mx[0] = fmaxf(mx[0], mx[a]);
-            const float m_new = fmaxf(m_run, mx[0] * sl2);
-            // a row that has seen no valid key yet keeps a finite base so no
+                for (int e = 0; e < 32; e += 2)
+                    mx[(e >> 1) & 3] = fmax3(mx[(e >> 1) & 3], __uint_as_float(sr[c][e]),
+                                             __uint_as_float(sr[c][e + 1]));
+            const float mrow = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+            const bool resc = mrow > r_base + kRescaleLog2;   // always true on the first valid tile
+            const float r_new = resc ? mrow : r_base;
+            // a row that has seen no valid key keeps a finite base, so no
             // -inf - (-inf) appears; its weights are then all zero
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ex2(m_run - m_use);  // 0 when m_run = -inf
-            const float nm = -m_use;
+            const float r_use = (r_new == -INFINITY) ? 0.f : r_new;
+            const float alpha = resc ? ex2(r_base - r_use) : 1.f;  // 0 when r_base = -inf
+            const float2 nr2 = make_float2(-r_use, -r_use);
+            const float2 sl22 = make_float2(sl2, sl2);
 
-            float ls[8];
+            float2 ls[4];
 #pragma unroll
-            for (int a = 0; a < 8; ++a) ls[a] = 0.f;
+            for (int a = 0; a < 4; ++a) ls[a] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const float w0 = ex2(fmaf(__uint_as_float(sr[c][e]), sl2, nm));
-                    const float w1 = ex2(fmaf(__uint_as_float(sr[c][e + 1]), sl2, nm));
-                    ls[e & 7] += w0;
-                    ls[(e + 1) & 7] += w1;
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(w0, w1);
+                    const float2 x = __ffma2_rn(
+                        make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sl22, nr2);
+                    const float2 w = make_float2(ex2(x.x), ex2(x.y));
+                    ls[(e >> 1) & 3] = __fadd2_rn(ls[(e >> 1) & 3], w);
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(w.x, w.y);
                     pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&pr);
                 }
                 // P columns 16c .. 16c+15 of this tile's S region
@@ -378,14 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st32(s_addr + 0, lo);
                 tmem_st32(s_addr + 32, hi);
             }
-            float rs = 0.f;
-#pragma unroll
-            for (int a = 0; a < 8; ++a) rs += ls[a];
-            l_run = l_run * alpha + rs;
-            m_run = m_new;
+            const float2 s01 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
+            l_run = fmaf(l_run, alpha, s01.x + s01.y);
+            r_base = r_new;
 
-            // correction: U <- alpha U (O holds PV(j-1) complete at this point)
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            // correction U <- alpha U, only when some row of the warp moved its
+            // base (O holds the complete PV(j-1) at this point)
+            if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
                 for (int c = 0; c < D / 32; c += 2) {
                     uint32_t o0[32], o1[32];
@@ -395,9 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     reg_fence(o0);
                     reg_fence(o1);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        o0[e] = __float_as_uint(__uint_as_float(o0[e]) * alpha);
-                        o1[e] = __float_as_uint(__uint_as_float(o1[e]) * alpha);
+                    for (int e = 0; e < 32; e += 2) {
+                        float2 v0 = __fmul2_rn(make_float2(__uint_as_float(o0[e]), __uint_as_float(o0[e + 1])), a2);
+                        float2 v1 = __fmul2_rn(make_float2(__uint_as_float(o1[e]), __uint_as_float(o1[e + 1])), a2);
+                        o0[e] = __float_as_uint(v0.x);
+                        o0[e + 1] = __float_as_uint(v0.y);
+                        o1[e] = __float_as_uint(v1.x);
+                        o1[e + 1] = __float_as_uint(v1.y);
                     }
                     tmem_st32(o_addr + c * 32, o0);
                     tmem_st32(o_addr + (c + 1) * 32, o1);
@@ -410,9 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ---- epilogue: O = U / l, L = m + log l
-        const bool have = ok && nkv[t] > 0;
+        const bool have = ok && my_nkv > 0;
         if (have) ok = wait_or_abort(bar_o_final(t), 0, p.err, kSiteO, abort_flag);
-        const bool store = qi < N && row0[t] < N;
+        const bool store = qi < N && my_row0 < N;
         __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.O) + (static_cast<size_t>(bh) * N + qi) * D;
         if (have && ok) {
             tc_fence_after();
@@ -440,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (store && p.L)
-                p.L[static_cast<size_t>(bh) * N + qi] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+                p.L[static_cast<size_t>(bh) * N + qi] = l_run > 0.f ? (r_base + __log2f(l_run)) * kLn2 : -INFINITY;
         } else if (!have && store) {
             // no valid key for this row (key_len = 0): O = 0, L = -inf
             uint4 *dst = reinterpret_cast<uint4 *>(orow);

@@ -244,6 +244,13 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
 }
 
 // ---------------------------------------------------------------- math
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // 2^x on the special-function unit (approximate, flushes denormals).
 __device__ __forceinline__ float ex2(float x) {
     float y;

@@ -32,9 +32,15 @@
 //     P = bf16(exp2(S*scale*log2e - m)) over the first half of S's TMEM
 //     columns, and rescale O in TMEM by alpha when some row's max moved.
 //     At the end they normalise O by 1/l and write O and L.
+//   Warps 8-11 form the third warpgroup (10 and 11 have no role); it hands
+//   registers to the softmax warpgroups with setmaxnreg so the softmax can
+//   hold a whole 128-column score row without spilling.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 after it.
 //
 // The MMA issue order per KV step is PV_0(j), S_0(j+1), PV_1(j), S_1(j+1):
+// (KV ring slots are released by a softmax thread once it sees S_t(j), which
+// covers every MMA that read K_j and V_{j-1}; a tcgen05.commit per release
+// would stall the MMA issue stream.)
 // S_t(j+1) overwrites the P_t(j) that PV_t(j) reads, which relies on the
 // tensor core executing one CTA's MMAs in issue order; and the barrier that
 // announces S_t(j+1) also covers PV_t(j), so the softmax may rescale O_t
@@ -55,8 +61,11 @@ constexpr int BM = 128;          // query rows per tile (MMA M)
 constexpr int BN = 128;          // keys per KV tile (MMA N of Q K^T, K of P V)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;        // 3 warpgroups: softmax 0, softmax 1, producer/MMA (+2 idle warps)
+constexpr int kRegsSoftmax = 208;    // per-thread registers of the softmax warpgroups after setmaxnreg
+constexpr int kRegsAux = 56;         // per-thread registers of the producer/MMA warpgroup
 constexpr int kTmemCols = 512;
+constexpr int kPrefetchTiles = 4;   // L2 prefetch distance of the KV stream, in KV tiles
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleLog2 = 8.0f;  // move the exponent base only when the max grows by > 2^8
 
@@ -175,133 +184,145 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kProducerWarp) {
-        // ================================================= TMA producer
-        if (lane == 0) {
-            prefetch_tmap(&tm.q);
-            prefetch_tmap(&tm.k);
-            prefetch_tmap(&tm.v);
-            const uint64_t pol_q = l2_policy_evict_first();
-            const uint64_t pol_kv = l2_policy_evict_normal();
-            mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
+    // Move registers from the producer/MMA warpgroup to the softmax warpgroups
+    // (the host checks 2*128*kRegsSoftmax + 128*kRegsAux <= 384 * launch registers).
+    if (warp >= 8) {
+        setmaxnreg_dec<kRegsAux>();
+        if (warp == kProducerWarp) {
+            // ================================================= TMA producer
+            if (lane == 0) {
+                prefetch_tmap(&tm.q);
+                prefetch_tmap(&tm.k);
+                prefetch_tmap(&tm.v);
+                const uint64_t pol_q = l2_policy_evict_first();
+                const uint64_t pol_kv = l2_policy_evict_normal();
+                mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
 #pragma unroll
-            for (int t = 0; t < 2; ++t)
-#pragma unroll
-                for (int cb = 0; cb < C::kColBlocks; ++cb)
-                    tma_load_3d(q_smem + t * C::kTileBytes + cb * (BM * 128), &tm.q, cb * 64, row0[t], bh,
-                                bar_q, pol_q);
-            int issued = 0;
-            for (int j = 0; j < ntot && !*abort_flag; ++j) {
-                for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
-                    const int item = 2 * j + kv;
-                    const int s = item % C::kSlots;
-                    if (item >= C::kSlots &&
-                        !wait_or_abort(bar_kv_empty(s), ((item / C::kSlots) - 1) & 1, p.err, kSiteKvEmpty,
-                                       abort_flag))
-                        break;
-                    mbar_arrive_expect_tx(bar_kv_full(s), C::kTileBytes);
-                    const CUtensorMap *map = kv ? &tm.v : &tm.k;
+                for (int t = 0; t < 2; ++t)
 #pragma unroll
                     for (int cb = 0; cb < C::kColBlocks; ++cb)
-                        tma_load_3d(ring + s * C::kTileBytes + cb * (BN * 128), map, cb * 64, j * BN, bh,
-                                    bar_kv_full(s), pol_kv);
-                    ++issued;
-                }
-            }
-            // Drain: no copy may still be in flight when the CTA exits.
-            mbar_wait(bar_q, 0, p.err, kSiteDrain);
-            const int first = issued > C::kSlots ? issued - C::kSlots : 0;
-            for (int item = first; item < issued; ++item)
-                mbar_wait(bar_kv_full(item % C::kSlots), (item / C::kSlots) & 1, p.err, kSiteDrain);
-        }
-    } else if (warp == kMmaWarp) {
-        // ================================================= MMA issuer
-        if (lane == 0 && ntot > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);
-            auto issue_s = [&](int t, uint32_t kslot) {
-                const uint32_t qa = q_smem + t * C::kTileBytes;
+                        tma_load_3d(q_smem + t * C::kTileBytes + cb * (BM * 128), &tm.q, cb * 64, row0[t], bh,
+                                    bar_q, pol_q);
+                // prime L2 with the first KV tiles
+                for (int j = 0; j < kPrefetchTiles && j < ntot; ++j)
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-                    mma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024),
-                           sdesc_sw128(kslot + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](int t, uint32_t vslot, int j) {
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
-                           sdesc_sw128(vslot + kk * 2048, BN * 128, 1024), idesc_o,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                }
-            };
-            bool ok = wait_or_abort(bar_q, 0, p.err, kSiteQ, abort_flag);
-            // prologue: S_t(0)
-            if (ok) ok = wait_or_abort(bar_kv_full(0), 0, p.err, kSiteKvFull, abort_flag);
-            if (ok) {
-                tc_fence_after();
-                for (int t = 0; t < 2; ++t)
-                    if (nkv[t] > 0) {
-                        issue_s(t, ring);
-                        mma_commit(bar_s_full(t));
+                    for (int cb = 0; cb < C::kColBlocks; ++cb) {
+                        tma_prefetch_3d(&tm.k, cb * 64, j * BN, bh);
+                        tma_prefetch_3d(&tm.v, cb * 64, j * BN, bh);
                     }
-                mma_commit(bar_kv_empty(0));
-            }
-            for (int j = 0; ok && j < ntot; ++j) {
-                const int iv = 2 * j + 1, ik = 2 * j + 2;
-                const int sv = iv % C::kSlots, sk = ik % C::kSlots;
-                const uint32_t vslot = ring + sv * C::kTileBytes;
-                const uint32_t kslot = ring + sk * C::kTileBytes;
-                const bool more = (j + 1 < ntot);
-                ok = wait_or_abort(bar_kv_full(sv), (iv / C::kSlots) & 1, p.err, kSiteKvFull, abort_flag);
-                bool k_ready = false;
+                int issued = 0;
+                for (int j = 0; j < ntot && !*abort_flag; ++j) {
+                    for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
+                        const int item = 2 * j + kv;
+                        const int s = item % C::kSlots;
+                        if (item >= C::kSlots &&
+                            !wait_or_abort(bar_kv_empty(s), ((item / C::kSlots) - 1) & 1, p.err, kSiteKvEmpty,
+                                           abort_flag))
+                            break;
+                        mbar_arrive_expect_tx(bar_kv_full(s), C::kTileBytes);
+                        const CUtensorMap *map = kv ? &tm.v : &tm.k;
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (!ok) break;
-                    if (j < nkv[t]) {
-                        ok = wait_or_abort(bar_p_ready(t), j & 1, p.err, kSiteP, abort_flag);
+                        for (int cb = 0; cb < C::kColBlocks; ++cb)
+                            tma_load_3d(ring + s * C::kTileBytes + cb * (BN * 128), map, cb * 64, j * BN, bh,
+                                        bar_kv_full(s), pol_kv);
+                        // Warm L2 with the same tensor's tile kPrefetchTiles steps
+                        // ahead: the CTAs of one head walk the KV tiles in step, so
+                        // a tile's first touch would otherwise stall them all on DRAM.
+                        if (j + kPrefetchTiles < ntot)
+#pragma unroll
+                            for (int cb = 0; cb < C::kColBlocks; ++cb)
+                                tma_prefetch_3d(map, cb * 64, (j + kPrefetchTiles) * BN, bh);
+                        ++issued;
+                    }
+                }
+                // Drain: no copy may still be in flight when the CTA exits.
+                mbar_wait(bar_q, 0, p.err, kSiteDrain);
+                const int first = issued > C::kSlots ? issued - C::kSlots : 0;
+                for (int item = first; item < issued; ++item)
+                    mbar_wait(bar_kv_full(item % C::kSlots), (item / C::kSlots) & 1, p.err, kSiteDrain);
+            }
+        } else if (warp == kMmaWarp) {
+            // ================================================= MMA issuer
+            if (lane == 0 && ntot > 0) {
+                constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
+                constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);
+                // A descriptor advanced by a byte offset: the start-address
+                // field holds address >> 4 and never carries (SMEM < 256 KB).
+                auto issue_s = [&](int t, uint32_t kslot) {
+                    const uint64_t qd = sdesc_sw128(q_smem + t * C::kTileBytes, 16, 1024);
+                    const uint64_t kd = sdesc_sw128(kslot, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+                        mma_ss(tmem + t * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                };
+                auto issue_pv = [&](int t, uint32_t vslot, int j) {
+                    const uint64_t vd = sdesc_sw128(vslot, BN * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, vd + ((kk * 2048) >> 4), idesc_o,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                };
+                bool ok = wait_or_abort(bar_q, 0, p.err, kSiteQ, abort_flag);
+                // prologue: S_t(0)
+                if (ok) ok = wait_or_abort(bar_kv_full(0), 0, p.err, kSiteKvFull, abort_flag);
+                if (ok) {
+                    tc_fence_after();
+                    for (int t = 0; t < 2; ++t)
+                        if (nkv[t] > 0) {
+                            issue_s(t, ring);
+                            mma_commit(bar_s_full(t));
+                        }
+                }
+                for (int j = 0; ok && j < ntot; ++j) {
+                    const int iv = 2 * j + 1, ik = 2 * j + 2;
+                    const int sv = iv % C::kSlots, sk = ik % C::kSlots;
+                    const uint32_t vslot = ring + sv * C::kTileBytes;
+                    const uint32_t kslot = ring + sk * C::kTileBytes;
+                    ok = wait_or_abort(bar_kv_full(sv), (iv / C::kSlots) & 1, p.err, kSiteKvFull, abort_flag);
+                    bool k_ready = false;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
                         if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(t, vslot, j);
-                        if (j + 1 == nkv[t]) mma_commit(bar_o_final(t));
-                    }
-                    if (t == 1) mma_commit(bar_kv_empty(sv));
-                    if (j + 1 < nkv[t]) {
-                        if (!k_ready) {
-                            ok = wait_or_abort(bar_kv_full(sk), (ik / C::kSlots) & 1, p.err, kSiteKvFull,
-                                               abort_flag);
+                        if (j < nkv[t]) {
+                            ok = wait_or_abort(bar_p_ready(t), j & 1, p.err, kSiteP, abort_flag);
                             if (!ok) break;
                             tc_fence_after();
-                            k_ready = true;
+                            issue_pv(t, vslot, j);
+                            if (j + 1 == nkv[t]) mma_commit(bar_o_final(t));
                         }
-                        issue_s(t, kslot);
-                        mma_commit(bar_s_full(t));
+                        if (j + 1 < nkv[t]) {
+                            if (!k_ready) {
+                                ok = wait_or_abort(bar_kv_full(sk), (ik / C::kSlots) & 1, p.err, kSiteKvFull,
+                                                   abort_flag);
+                                if (!ok) break;
+                                tc_fence_after();
+                                k_ready = true;
+                            }
+                            issue_s(t, kslot);
+                            mma_commit(bar_s_full(t));
+                        }
                     }
-                }
-                if (ok && more) {
-                    if (!k_ready) {
-                        // no tile needed K_{j+1}: still consume the slot
-                        ok = wait_or_abort(bar_kv_full(sk), (ik / C::kSlots) & 1, p.err, kSiteKvFull,
-                                           abort_flag);
-                    }
-                    mma_commit(bar_kv_empty(sk));
                 }
             }
-        }
-        if (lane == 0 && ntot > 0) {
-            // every MMA issued above has completed before TMEM is released
-            mma_commit(bar_mma_done);
-            mbar_wait(bar_mma_done, 0, p.err, kSiteMmaDone);
-        }
-        __syncwarp();
+            if (lane == 0 && ntot > 0) {
+                // every MMA issued above has completed before TMEM is released
+                mma_commit(bar_mma_done);
+                mbar_wait(bar_mma_done, 0, p.err, kSiteMmaDone);
+            }
+            __syncwarp();
+        }  // warps 10, 11: no role
     } else {
+        setmaxnreg_inc<kRegsSoftmax>();
         // ================================================= softmax warpgroups
         const int t = warp >> 2;              // query tile of this warpgroup
         const int quarter = warp & 3;         // TMEM lane quarter
         const int r = quarter * 32 + lane;    // row within the tile
         const int my_row0 = t ? row0[1] : row0[0];
         const int my_nkv = t ? nkv[1] : nkv[0];
+        const int t_rel = nkv[1] > 0 ? 1 : 0;  // tile whose S completion releases KV slots
         const int qi = my_row0 + r;           // query index
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + t * 128;
@@ -319,6 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < my_nkv; ++j) {
             ok = wait_or_abort(bar_s_full(t), j & 1, p.err, kSiteS, abort_flag);
             if (!ok) break;
+            // S_t(j) complete implies every MMA issued before it is complete:
+            // the releasing tile (the one active for every KV step) hands K_j
+            // and V_{j-1} back to the producer with a plain arrive.
+            if (t == t_rel && quarter == 0 && lane == 0) {
+                mbar_arrive(bar_kv_empty((2 * j) % C::kSlots));
+                if (j > 0) mbar_arrive(bar_kv_empty((2 * j - 1) % C::kSlots));
+            }
             tc_fence_after();
             __syncwarp();
             uint32_t sr[4][32];
@@ -516,6 +544,18 @@ cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
     const int smem = Cfg<D>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // setmaxnreg.inc only completes when the registers it asks for exist in
+    // the block's launch allocation: refuse to launch a build where they do not.
+    static int regs_ok = -1;
+    if (regs_ok < 0) {
+        cudaFuncAttributes fa_attr;
+        e = cudaFuncGetAttributes(&fa_attr, prefill_kernel<D>);
+        if (e != cudaSuccess) return e;
+        const long long have = static_cast<long long>(fa_attr.numRegs) * kThreads;
+        const long long want = 2ll * 128 * kRegsSoftmax + 128ll * kRegsAux;
+        regs_ok = (have >= want && fa_attr.numRegs >= kRegsAux && fa_attr.numRegs <= kRegsSoftmax) ? 1 : 0;
+    }
+    if (!regs_ok) return cudaErrorInvalidConfiguration;
     const int npairs = (p.N + 2 * BM - 1) / (2 * BM);
     dim3 grid(npairs, p.H, p.B);
     prefill_kernel<D><<<grid, kThreads, smem, stream>>>(tm, p);

@@ -114,6 +114,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// L2 prefetch of one tiled 3-D box (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0),
+                 "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -241,6 +248,17 @@ template <int N>
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
 #pragma unroll
     for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// ---------------------------------------------------------------- registers
+// Per-warpgroup register re-allocation; every warp of the warpgroup executes it.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------- math

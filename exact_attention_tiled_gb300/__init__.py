@@ -55,6 +55,9 @@ def library():
         lib.fa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float, _i,
                                   _vp, ctypes.c_size_t, _vp]
         lib.fa_decode.restype = _i
+        lib.fa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float,
+                                          _i, _vp]
+        lib.fa_decode_noalloc.restype = _i
         lib.fa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _vp]
         lib.fa_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_decode_plan.argtypes = [_i, _i, _i, _i, _i, _vp, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]

@@ -140,6 +140,38 @@ FA_API fa_status fa_decode_plan(int B, int H, int Lmax, int d, int num_splits,
                          const int32_t *seqlens_host, int num_sms,
                          int *chunk_len, int *max_chunks);
 
+/*
+ * fa_decode_noalloc -- fa_decode for callers that cannot allocate device
+ * memory when they decode (a runtime that gives all device memory to its
+ * own pool at start-up and forbids later allocations, a plugin whose host
+ * application owns the memory budget, a token loop where cudaMalloc or
+ * cudaFree could synchronise the device).  The pages have no counterpart of
+ * this entry point; it only changes where the split partials are kept.
+ *
+ * Arguments and results are those of fa_decode without `workspace` and
+ * `workspace_bytes`: the partials go to one array of
+ * FA_DECODE_NOALLOC_MAX_BYTES that the library keeps in device memory on
+ * every GPU that loads it, until the process exits.  The call allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ *   - A request whose fa_decode_workspace_bytes() exceeds
+ *     FA_DECODE_NOALLOC_MAX_BYTES returns FA_ERR_WORKSPACE and launches
+ *     nothing; use fa_decode with your own workspace for it.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device uses the same array.  Nothing in it needs to
+ *     start at zero (each partial is written before it is read), but two
+ *     calls that overlap on the GPU, e.g. on two streams, race on it: order
+ *     them on one stream or with events.
+ */
+#define FA_DECODE_NOALLOC_MAX_BYTES (8u << 20) /* 8 MiB */
+
+FA_API fa_status fa_decode_noalloc(const void *q, const void *Kcache, const void *Vcache,
+                                   const int32_t *seqlens, const int32_t *seqlens_host,
+                                   void *O, float *L,
+                                   int B, int H, int Lmax, int d, float scale, int num_splits,
+                                   fa_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 FA_API const char *fa_status_string(fa_status s);
 

@@ -61,10 +61,17 @@ def load_peaks():
                 "source": "fallback"}
 
 
-def kernel_sources_hash():
+KERNEL_SOURCES = {
+    "prefill_kernel": ("fa_prefill.cu", "fa_ptx.cuh", "fa_internal.h"),
+    "decode_split_kernel": ("fa_decode.cu", "fa_ptx.cuh", "fa_internal.h"),
+}
+
+
+def kernel_sources_hash(kernel):
+    """Hash of the source files a kernel is compiled from (stale counters read as null)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_tiled_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -80,7 +87,7 @@ def recorded_traffic(kernel):
     except Exception:
         return None
     ent = rec.get(kernel)
-    if not ent or ent.get("sources_sha") != kernel_sources_hash():
+    if not ent or ent.get("sources_sha") != kernel_sources_hash(kernel):
         return None
     return ent.get("bytes_per_launch")
 
@@ -237,6 +244,45 @@ def run_ours(args, rank, world, local_rank):
         sweep["auto" if splits == 0 else str(splits)] = round(
             decode_bytes(wd.H, seqlens.tolist(), wd.d) / (statistics.mean(ts) * 1e-3) / 1e9, 1)
 
+    # ---- the other two workload shapes, timed the same way (reported, not the headline)
+    def timed(fn, iters=10, warm=3):
+        ts = []
+        for i in range(warm + iters):
+            flush.fill_(5)
+            a, b = ev(), ev()
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= warm:
+                ts.append(a.elapsed_time(b))
+        return statistics.mean(ts)
+
+    others = {}
+    w3 = workloads.WORKLOADS["prefill_b8h16_n2048_d64"]
+    Q3, K3, V3 = workloads.prefill_inputs(w3.B, w3.H, w3.N, w3.d, w3.seed, w3.amp, device=dev)
+    kl3 = workloads.key_lengths(w3.B, w3.N, w3.key_len_seed)
+    kl3d = kl3.to(dev)
+    for name, kl in (("prefill_b8h16_n2048_d64", None), ("prefill_b8h16_n2048_d64_keypad", kl3d)):
+        ms = timed(lambda: fa.fa_forward(Q3, K3, V3, causal=False, key_len=kl))
+        fl = prefill_flops(w3.B, w3.H, w3.N, w3.d, False) if kl is None else \
+            4.0 * w3.d * w3.N * float(kl3.sum()) * w3.H
+        others[name] = {"ms": round(ms, 4), "flops": fl, "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+                        "frac_of_bf16_peak": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+    del Q3, K3, V3
+    w5 = workloads.WORKLOADS["decode_varlen_b16h32_d128"]
+    q5, K5, V5 = workloads.decode_inputs(w5.B, w5.H, w5.N, w5.d, w5.seed, device=dev)
+    sl5 = workloads.decode_seqlens(w5.B, w5.N, w5.seed, w5.seqlen_range)
+    sl5d = sl5.to(dev)
+    ws5 = torch.empty(fa.fa_decode_workspace_bytes(w5.B, w5.H, w5.N, w5.d, 0, sl5), device=dev, dtype=torch.uint8)
+    ms = timed(lambda: fa.fa_decode(q5, K5, V5, sl5d, num_splits=0, seqlens_host=sl5, workspace=ws5))
+    by5 = decode_bytes(w5.H, sl5.tolist(), w5.d)
+    c5, n5 = fa.fa_decode_plan(w5.B, w5.H, w5.N, w5.d, 0, sl5)
+    others["decode_varlen_b16h32_d128"] = {"ms": round(ms, 4), "bytes": by5, "gbs": round(by5 / (ms * 1e-3) / 1e9, 1),
+                                           "frac_of_hbm_peak": round(by5 / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                                           "chunk_len": c5, "max_chunks": n5}
+    del q5, K5, V5
+
     # ---- end to end through the public call with host buffers
     Qh, Kh, Vh = (t.cpu().pin_memory() for t in (Q, K, V))
     Oh = torch.empty(O.shape, dtype=O.dtype).pin_memory()
@@ -310,6 +356,7 @@ def run_ours(args, rank, world, local_rank):
                                 "peak_source": f"HBM copy, of {src}",
                                 "traffic": recorded_traffic("decode_split_kernel"),
                                 "kernel": "decode_split_kernel<128> + decode_merge_kernel<128>"}},
+        "other_workloads": others,
         "gpu_launches": launches,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 3),
@@ -378,6 +425,33 @@ def run_reference(args):
     }
 
 
+def record_traffic(report, kernel, units_note):
+    """Store DRAM bytes per launch of `kernel` from an ncu report into profiles/dram_traffic.json."""
+    out = subprocess.run(["ncu", "-i", report, "--page", "raw", "--csv"], capture_output=True, text=True,
+                         check=True).stdout
+    import csv
+    rows = list(csv.reader(out.splitlines()))
+    hdr, data = rows[0], rows[2:]
+    name_i = hdr.index("Kernel Name")
+    rd, wr = hdr.index("dram__bytes_read.sum"), hdr.index("dram__bytes_write.sum")
+    units = rows[1]
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    vals = [float(r[rd].replace(",", "")) * scale[units[rd]] + float(r[wr].replace(",", "")) * scale[units[wr]]
+            for r in data if kernel in r[name_i]]
+    if not vals:
+        raise SystemExit(f"no launch of {kernel} in {report}")
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    rec = {}
+    if os.path.exists(path):
+        with open(path) as f:
+            rec = json.load(f)
+    rec[kernel] = {"bytes_per_launch": statistics.mean(vals), "launches": len(vals),
+                   "sources_sha": kernel_sources_hash(kernel), "note": units_note}
+    with open(path, "w") as f:
+        json.dump(rec, f, indent=1, sort_keys=True)
+    print(json.dumps(rec[kernel]))
+
+
 def run_profile_case(args):
     """Warm-up launches plus `steps` launches of one kernel, nothing else (for ncu)."""
     import torch
@@ -413,7 +487,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
                     help="only launch one kernel warmup+steps times (for ncu captures)")
+    ap.add_argument("--record-traffic", nargs=3, metavar=("REPORT", "KERNEL", "NOTE"), default=None,
+                    help="write DRAM bytes per launch of KERNEL from an ncu report to profiles/")
     args = ap.parse_args()
+    if args.record_traffic:
+        record_traffic(*args.record_traffic)
+        return
     if args.profile:
         run_profile_case(args)
         return

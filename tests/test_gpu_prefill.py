@@ -104,3 +104,18 @@ def test_causal_8k_d128_sampled():
 def test_prefill_no_device_error_recorded():
     st, site = fa().fa_device_error(clear=True)
     assert st == 0, f"bounded wait ran out at site {site:#x}"
+
+
+@pytest.mark.parametrize("d,causal", [(128, False), (64, True), (128, True)])
+def test_late_max_jump_rebases_and_rescales(d, causal):
+    """Keys in later KV tiles with much larger scores force the exponent base to
+    move after the first tile (the recompute-and-rescale path of the softmax)."""
+    B, H, N = 1, 2, 700
+    Q, K, V = workloads.prefill_inputs(B, H, N, d, seed=77)
+    K = K.float()
+    K[:, :, 300:420] *= 6.0          # scores ~6x larger from the third KV tile on
+    K[:, :, 600:] *= 12.0            # and again in the last tile
+    K = K.to(torch.bfloat16)
+    O, L = _fwd(Q, K, V, causal)
+    Oref, Lref = oracle.sdpa_forward(Q, K, V, causal=causal)
+    compare(f"max jump d{d} c{int(causal)}", O, L, Oref, Lref)

@@ -20,19 +20,19 @@
 // on the same page, section "FlashAttention-4": two query tiles per CTA so
 // the tensor core works on one tile's GEMM while the other tile's softmax
 // runs):
-//   * warp 8, one lane: TMA producer.  Loads Q for both query tiles once,
+//   * warp 0, one lane: TMA producer.  Loads Q for both query tiles once,
 //     then streams K_0, V_0, K_1, V_1, ... through a ring of shared-memory
 //     slots (128-byte swizzled, 64-column boxes).
-//   * warp 9: allocates tensor memory; one lane issues every tcgen05.mma:
+//   * warp 1: allocates tensor memory; one lane issues every tcgen05.mma:
 //       S_t = Q_t K_j^T        (A, B from shared memory, fp32 into TMEM)
 //       O_t += P_t V_j         (A = P from TMEM, B = V from shared memory)
 //     and signals completion through tcgen05.commit -> mbarrier.
-//   * warps 0-3 / 4-7: softmax warpgroups for query tile 0 / 1, one thread
+//   * warps 4-7 / 8-11: softmax warpgroups for query tile 0 / 1, one thread
 //     per query row.  They read S from TMEM, mask, update (m, l), write
 //     P = bf16(exp2(S*scale*log2e - m)) over the first half of S's TMEM
 //     columns, and rescale O in TMEM by alpha when some row's max moved.
 //     At the end they normalise O by 1/l and write O and L.
-//   Warps 8-11 form the third warpgroup (10 and 11 have no role); it hands
+//   Warps 0-3 form the first warpgroup (2 and 3 have no role); it hands
 //   registers to the softmax warpgroups with setmaxnreg so the softmax can
 //   hold a whole 128-column score row without spilling.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 after it.
@@ -59,11 +59,11 @@ namespace {
 
 constexpr int BM = 128;          // query rows per tile (MMA M)
 constexpr int BN = 128;          // keys per KV tile (MMA N of Q K^T, K of P V)
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
 constexpr int kThreads = 384;        // 3 warpgroups: softmax 0, softmax 1, producer/MMA (+2 idle warps)
-constexpr int kRegsSoftmax = 208;    // per-thread registers of the softmax warpgroups after setmaxnreg
-constexpr int kRegsAux = 56;         // per-thread registers of the producer/MMA warpgroup
+constexpr int kRegsSoftmax = 216;    // per-thread registers of the softmax warpgroups after setmaxnreg
+constexpr int kRegsAux = 72;         // per-thread registers of the producer/MMA warpgroup
 constexpr int kTmemCols = 512;
 constexpr int kPrefetchTiles = 4;   // L2 prefetch distance of the KV stream, in KV tiles
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -82,8 +82,9 @@ struct Cfg {
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
-    // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_ready[2], o_final[2], mma_done
-    static constexpr int kNumBars = 1 + 2 * kSlots + 7;
+    // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_ready[2], o_final[2], mma_done,
+    //           q_free, o_free[2]
+    static constexpr int kNumBars = 1 + 2 * kSlots + 10;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;    // tmem base + abort flag
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // +1024 for base alignment
 };
@@ -107,9 +108,51 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uns
     }
 }
 
+// One work item = one (b, h, pair of 128-row query tiles).
+struct Item {
+    int b, h, bh, klen, ntot, t_rel;
+    int row0[2], nkv[2];
+};
+
+__device__ __forceinline__ Item item_info(const PrefillParams &p, int k, int npairs) {
+    Item it;
+    const int units = p.B * p.H;
+    // heaviest causal pairs first, all heads of a pair index together
+    const int pair = npairs - 1 - k / units;
+    it.bh = k % units;
+    it.b = it.bh / p.H;
+    it.h = it.bh % p.H;
+    const int N = p.N;
+    it.klen = N;
+    if (p.key_len) {
+        const int v = p.key_len[it.b];
+        it.klen = v < 0 ? 0 : (v > N ? N : v);
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        it.row0[t] = pair * 2 * BM + t * BM;
+        if (it.row0[t] >= N) {
+            it.nkv[t] = 0;
+            continue;
+        }
+        int kend = it.klen;
+        if (p.causal) kend = min(kend, min(N, it.row0[t] + BM));
+        it.nkv[t] = (kend + BN - 1) / BN;
+    }
+    it.ntot = max(it.nkv[0], it.nkv[1]);
+    it.t_rel = it.nkv[1] > 0 ? 1 : 0;  // the tile active in every KV step of the item
+    return it;
+}
+
+// Static schedule of a persistent CTA: round r takes item r*G + c, or
+// r*G + G-1-c on odd rounds, so the heavy-first order is dealt out evenly.
+__device__ __forceinline__ int item_of_round(int r, int G, int c) {
+    return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ TmapSet tm, const PrefillParams p) {
+    prefill_kernel(const __grid_constant__ TmapSet tm, const PrefillParams p, int num_items, int npairs) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzled tiles need 1024-byte aligned bases.
@@ -126,38 +169,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_p_ready = [&](int t) { return bars + 8u * (3 + 2 * C::kSlots + t); };
     auto bar_o_final = [&](int t) { return bars + 8u * (5 + 2 * C::kSlots + t); };
     const uint32_t bar_mma_done = bars + 8u * (7 + 2 * C::kSlots);
+    const uint32_t bar_q_free = bars + 8u * (8 + 2 * C::kSlots);
+    auto bar_o_free = [&](int t) { return bars + 8u * (9 + 2 * C::kSlots + t); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int npairs = gridDim.x;
-    const int pair = npairs - 1 - static_cast<int>(blockIdx.x);  // heaviest causal pairs first
-    const int bh = b * p.H + h;
+    const int G = gridDim.x, cta = blockIdx.x;
     const int N = p.N;
-
-    // ---- per-CTA work bounds (identical in every thread)
-    int klen = N;
-    if (p.key_len) {
-        const int v = p.key_len[b];
-        klen = v < 0 ? 0 : (v > N ? N : v);
-    }
-    int row0[2], nkv[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        row0[t] = pair * 2 * BM + t * BM;
-        if (row0[t] >= N) {
-            nkv[t] = 0;
-            continue;
-        }
-        int kend = klen;
-        if (p.causal) {
-            const int qend = min(N, row0[t] + BM);
-            kend = min(kend, qend);
-        }
-        nkv[t] = (kend + BN - 1) / BN;
-    }
-    const int ntot = max(nkv[0], nkv[1]);
 
     // ---- set-up: barriers, TMEM
     if (threadIdx.x == 0) {
@@ -170,8 +189,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_s_full(t), 1);
             mbar_init(bar_p_ready(t), 4);
             mbar_init(bar_o_final(t), 1);
+            mbar_init(bar_o_free(t), 4);
         }
         mbar_init(bar_mma_done, 1);
+        mbar_init(bar_q_free, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -186,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Move registers from the producer/MMA warpgroup to the softmax warpgroups
     // (the host checks 2*128*kRegsSoftmax + 128*kRegsAux <= 384 * launch registers).
-    if (warp >= 8) {
+    if (warp < 4) {
         setmaxnreg_dec<kRegsAux>();
         if (warp == kProducerWarp) {
             // ================================================= TMA producer
@@ -196,54 +217,76 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prefetch_tmap(&tm.v);
                 const uint64_t pol_q = l2_policy_evict_first();
                 const uint64_t pol_kv = l2_policy_evict_normal();
-                mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
+                int g = 0;       // running index of K/V tiles in the ring (all items)
+                int qi = 0;      // items with work so far (phase of q_full / q_free)
+                bool ok = true;
+                for (int r = 0; ok; ++r) {
+                    const int k = item_of_round(r, G, cta);
+                    if (k >= num_items) break;
+                    const Item it = item_info(p, k, npairs);
+                    if (it.ntot == 0) continue;
+                    // Q of the next item of this CTA: warm L2 while this one runs
+                    const int kn = item_of_round(r + 1, G, cta);
+                    if (kn < num_items) {
+                        const Item nx = item_info(p, kn, npairs);
 #pragma unroll
-                for (int t = 0; t < 2; ++t)
-#pragma unroll
-                    for (int cb = 0; cb < C::kColBlocks; ++cb)
-                        tma_load_3d(q_smem + t * C::kTileBytes + cb * (BM * 128), &tm.q, cb * 64, row0[t], bh,
-                                    bar_q, pol_q);
-                // prime L2 with the first KV tiles
-                for (int j = 0; j < kPrefetchTiles && j < ntot; ++j)
-#pragma unroll
-                    for (int cb = 0; cb < C::kColBlocks; ++cb) {
-                        tma_prefetch_3d(&tm.k, cb * 64, j * BN, bh);
-                        tma_prefetch_3d(&tm.v, cb * 64, j * BN, bh);
-                    }
-                int issued = 0;
-                for (int j = 0; j < ntot && !*abort_flag; ++j) {
-                    for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
-                        const int item = 2 * j + kv;
-                        const int s = item % C::kSlots;
-                        if (item >= C::kSlots &&
-                            !wait_or_abort(bar_kv_empty(s), ((item / C::kSlots) - 1) & 1, p.err, kSiteKvEmpty,
-                                           abort_flag))
-                            break;
-                        mbar_arrive_expect_tx(bar_kv_full(s), C::kTileBytes);
-                        const CUtensorMap *map = kv ? &tm.v : &tm.k;
-#pragma unroll
-                        for (int cb = 0; cb < C::kColBlocks; ++cb)
-                            tma_load_3d(ring + s * C::kTileBytes + cb * (BN * 128), map, cb * 64, j * BN, bh,
-                                        bar_kv_full(s), pol_kv);
-                        // Warm L2 with the same tensor's tile kPrefetchTiles steps
-                        // ahead: the CTAs of one head walk the KV tiles in step, so
-                        // a tile's first touch would otherwise stall them all on DRAM.
-                        if (j + kPrefetchTiles < ntot)
+                        for (int t = 0; t < 2; ++t)
 #pragma unroll
                             for (int cb = 0; cb < C::kColBlocks; ++cb)
-                                tma_prefetch_3d(map, cb * 64, (j + kPrefetchTiles) * BN, bh);
-                        ++issued;
+                                tma_prefetch_3d(&tm.q, cb * 64, nx.row0[t], nx.bh);
+                    }
+                    // Q smem is free once the previous item's last S MMA completed
+                    if (qi > 0 && !wait_or_abort(bar_q_free, (qi - 1) & 1, p.err, kSiteQ, abort_flag)) break;
+                    mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int cb = 0; cb < C::kColBlocks; ++cb)
+                            tma_load_3d(q_smem + t * C::kTileBytes + cb * (BM * 128), &tm.q, cb * 64, it.row0[t],
+                                        it.bh, bar_q, pol_q);
+                    ++qi;
+                    for (int j = 0; j < kPrefetchTiles && j < it.ntot; ++j)
+#pragma unroll
+                        for (int cb = 0; cb < C::kColBlocks; ++cb) {
+                            tma_prefetch_3d(&tm.k, cb * 64, j * BN, it.bh);
+                            tma_prefetch_3d(&tm.v, cb * 64, j * BN, it.bh);
+                        }
+                    for (int j = 0; ok && j < it.ntot; ++j) {
+                        for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
+                            const int s = g % C::kSlots;
+                            if (g >= C::kSlots &&
+                                !wait_or_abort(bar_kv_empty(s), ((g / C::kSlots) - 1) & 1, p.err, kSiteKvEmpty,
+                                               abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(bar_kv_full(s), C::kTileBytes);
+                            const CUtensorMap *map = kv ? &tm.v : &tm.k;
+#pragma unroll
+                            for (int cb = 0; cb < C::kColBlocks; ++cb)
+                                tma_load_3d(ring + s * C::kTileBytes + cb * (BN * 128), map, cb * 64, j * BN,
+                                            it.bh, bar_kv_full(s), pol_kv);
+                            // Warm L2 with the same tensor's tile kPrefetchTiles steps
+                            // ahead: the CTAs of one head walk the KV tiles in step, so
+                            // a tile's first touch would otherwise stall them on DRAM.
+                            if (j + kPrefetchTiles < it.ntot)
+#pragma unroll
+                                for (int cb = 0; cb < C::kColBlocks; ++cb)
+                                    tma_prefetch_3d(map, cb * 64, (j + kPrefetchTiles) * BN, it.bh);
+                            ++g;
+                        }
                     }
                 }
                 // Drain: no copy may still be in flight when the CTA exits.
-                mbar_wait(bar_q, 0, p.err, kSiteDrain);
-                const int first = issued > C::kSlots ? issued - C::kSlots : 0;
-                for (int item = first; item < issued; ++item)
+                if (qi > 0) mbar_wait(bar_q, (qi - 1) & 1, p.err, kSiteDrain);
+                const int first = g > C::kSlots ? g - C::kSlots : 0;
+                for (int item = first; item < g; ++item)
                     mbar_wait(bar_kv_full(item % C::kSlots), (item / C::kSlots) & 1, p.err, kSiteDrain);
             }
         } else if (warp == kMmaWarp) {
             // ================================================= MMA issuer
-            if (lane == 0 && ntot > 0) {
+            bool issued_any = false;
+            if (lane == 0) {
                 constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
                 constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);
                 // A descriptor advanced by a byte offset: the start-address
@@ -265,230 +308,280 @@ __global__ void __launch_bounds__(kThreads, 1)
                                (j > 0 || kk > 0) ? 1u : 0u);
                     }
                 };
-                bool ok = wait_or_abort(bar_q, 0, p.err, kSiteQ, abort_flag);
-                // prologue: S_t(0)
-                if (ok) ok = wait_or_abort(bar_kv_full(0), 0, p.err, kSiteKvFull, abort_flag);
-                if (ok) {
+                int g = 0;                 // running ring index of this item's K_0
+                int qi = 0;                // items with work so far
+                int pcnt[2] = {0, 0};      // PV_t issued so far (phase of p_ready[t])
+                int uses[2] = {0, 0};      // items in which tile t had work (o_final / o_free phases)
+                bool ok = true;
+                for (int r = 0; ok; ++r) {
+                    const int k = item_of_round(r, G, cta);
+                    if (k >= num_items) break;
+                    const Item it = item_info(p, k, npairs);
+                    if (it.ntot == 0) continue;
+                    ok = wait_or_abort(bar_q, qi & 1, p.err, kSiteQ, abort_flag);
+                    if (ok) ok = wait_or_abort(bar_kv_full(g % C::kSlots), (g / C::kSlots) & 1, p.err, kSiteKvFull,
+                                               abort_flag);
+                    if (!ok) break;
                     tc_fence_after();
-                    for (int t = 0; t < 2; ++t)
-                        if (nkv[t] > 0) {
-                            issue_s(t, ring);
-                            mma_commit(bar_s_full(t));
-                        }
-                }
-                for (int j = 0; ok && j < ntot; ++j) {
-                    const int iv = 2 * j + 1, ik = 2 * j + 2;
-                    const int sv = iv % C::kSlots, sk = ik % C::kSlots;
-                    const uint32_t vslot = ring + sv * C::kTileBytes;
-                    const uint32_t kslot = ring + sk * C::kTileBytes;
-                    ok = wait_or_abort(bar_kv_full(sv), (iv / C::kSlots) & 1, p.err, kSiteKvFull, abort_flag);
-                    bool k_ready = false;
+                    // S_t(0) may overwrite the previous item's P_t: its PV was issued earlier.
 #pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        if (!ok) break;
-                        if (j < nkv[t]) {
-                            ok = wait_or_abort(bar_p_ready(t), j & 1, p.err, kSiteP, abort_flag);
-                            if (!ok) break;
-                            tc_fence_after();
-                            issue_pv(t, vslot, j);
-                            if (j + 1 == nkv[t]) mma_commit(bar_o_final(t));
-                        }
-                        if (j + 1 < nkv[t]) {
-                            if (!k_ready) {
-                                ok = wait_or_abort(bar_kv_full(sk), (ik / C::kSlots) & 1, p.err, kSiteKvFull,
-                                                   abort_flag);
-                                if (!ok) break;
-                                tc_fence_after();
-                                k_ready = true;
-                            }
-                            issue_s(t, kslot);
+                    for (int t = 0; t < 2; ++t)
+                        if (it.nkv[t] > 0) {
+                            issue_s(t, ring + (g % C::kSlots) * C::kTileBytes);
                             mma_commit(bar_s_full(t));
                         }
+                    issued_any = true;
+                    if (it.ntot == 1) mma_commit(bar_q_free);  // the item's last S MMA is issued
+                    for (int j = 0; ok && j < it.ntot; ++j) {
+                        const int iv = g + 2 * j + 1, ik = g + 2 * j + 2;
+                        const int sv = iv % C::kSlots, sk = ik % C::kSlots;
+                        const uint32_t vslot = ring + sv * C::kTileBytes;
+                        const uint32_t kslot = ring + sk * C::kTileBytes;
+                        ok = wait_or_abort(bar_kv_full(sv), (iv / C::kSlots) & 1, p.err, kSiteKvFull, abort_flag);
+                        bool k_ready = false;
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            if (!ok) break;
+                            if (j < it.nkv[t]) {
+                                // O_t is overwritten by PV_t(0): the previous item's epilogue must have read it
+                                if (j == 0 && uses[t] > 0) {
+                                    ok = wait_or_abort(bar_o_free(t), (uses[t] - 1) & 1, p.err, kSiteO, abort_flag);
+                                    if (!ok) break;
+                                }
+                                ok = wait_or_abort(bar_p_ready(t), pcnt[t] & 1, p.err, kSiteP, abort_flag);
+                                if (!ok) break;
+                                ++pcnt[t];
+                                tc_fence_after();
+                                issue_pv(t, vslot, j);
+                                if (j + 1 == it.nkv[t]) mma_commit(bar_o_final(t));
+                            }
+                            if (j + 1 < it.nkv[t]) {
+                                if (!k_ready) {
+                                    ok = wait_or_abort(bar_kv_full(sk), (ik / C::kSlots) & 1, p.err, kSiteKvFull,
+                                                       abort_flag);
+                                    if (!ok) break;
+                                    tc_fence_after();
+                                    k_ready = true;
+                                }
+                                issue_s(t, kslot);
+                                mma_commit(bar_s_full(t));
+                            }
+                        }
+                        if (ok && j + 2 == it.ntot) mma_commit(bar_q_free);  // last S MMA of the item issued
                     }
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+                        if (it.nkv[t] > 0) ++uses[t];
+                    g += 2 * it.ntot;
+                    ++qi;
                 }
-            }
-            if (lane == 0 && ntot > 0) {
-                // every MMA issued above has completed before TMEM is released
-                mma_commit(bar_mma_done);
-                mbar_wait(bar_mma_done, 0, p.err, kSiteMmaDone);
+                if (issued_any) {
+                    // every MMA issued above has completed before TMEM is released
+                    mma_commit(bar_mma_done);
+                    mbar_wait(bar_mma_done, 0, p.err, kSiteMmaDone);
+                }
             }
             __syncwarp();
-        }  // warps 10, 11: no role
+        }  // warps 2, 3: no role
     } else {
         setmaxnreg_inc<kRegsSoftmax>();
         // ================================================= softmax warpgroups
-        const int t = warp >> 2;              // query tile of this warpgroup
+        const int t = (warp >> 2) - 1;        // query tile of this warpgroup
         const int quarter = warp & 3;         // TMEM lane quarter
         const int r = quarter * 32 + lane;    // row within the tile
-        const int my_row0 = t ? row0[1] : row0[0];
-        const int my_nkv = t ? nkv[1] : nkv[0];
-        const int t_rel = nkv[1] > 0 ? 1 : 0;  // tile whose S completion releases KV slots
-        const int qi = my_row0 + r;           // query index
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + t * 128;
         const uint32_t o_addr = tmem + lane_off + 256 + t * D;
         const float sl2 = p.scale_log2;
-
-        // Conditional rescaling ("Infra: Flash Attention", "Conditional
-        // rescaling invariant"): l and U are kept relative to a base r that
-        // only moves when the row max exceeds r + kRescaleLog2; u(r)/l(r) does
-        // not depend on r, and with r within kRescaleLog2 of the max every
-        // weight stays <= 2^kRescaleLog2.  r is in log2 units of the scaled score.
-        float r_base = -INFINITY;
-        float l_run = 0.f;
+        int scnt = 0;   // S_t completions consumed (phase of s_full[t])
+        int uses = 0;   // items in which this tile had work (phase of o_final[t])
+        int g = 0;      // running ring index of the item's K_0
         bool ok = true;
-        for (int j = 0; j < my_nkv; ++j) {
-            ok = wait_or_abort(bar_s_full(t), j & 1, p.err, kSiteS, abort_flag);
-            if (!ok) break;
-            // S_t(j) complete implies every MMA issued before it is complete:
-            // the releasing tile (the one active for every KV step) hands K_j
-            // and V_{j-1} back to the producer with a plain arrive.
-            if (t == t_rel && quarter == 0 && lane == 0) {
-                mbar_arrive(bar_kv_empty((2 * j) % C::kSlots));
-                if (j > 0) mbar_arrive(bar_kv_empty((2 * j - 1) % C::kSlots));
-            }
-            tc_fence_after();
-            __syncwarp();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+        for (int rr = 0; ok; ++rr) {
+            const int k = item_of_round(rr, G, cta);
+            if (k >= num_items) break;
+            const Item it = item_info(p, k, npairs);
+            const int my_row0 = t ? it.row0[1] : it.row0[0];
+            const int my_nkv = t ? it.nkv[1] : it.nkv[0];
+            const int klen = it.klen;
+            const int qi = my_row0 + r;           // query index
+            const bool store = qi < N && my_row0 < N;
+            __nv_bfloat16 *orow =
+                static_cast<__nv_bfloat16 *>(p.O) + (static_cast<size_t>(it.bh) * N + qi) * D;
 
-            // mask: keys beyond key_len / the sequence, and the causal future
-            const int kbase = j * BN;
-            const bool need_mask = (kbase + BN > klen) || (p.causal && kbase + BN > my_row0);
-            if (need_mask) {
-                int lim = klen - kbase;
-                if (p.causal) lim = min(lim, qi - kbase + 1);
+            // Conditional rescaling ("Infra: Flash Attention", "Conditional
+            // rescaling invariant"): l and U are kept relative to a base r that
+            // only moves when the row max exceeds r + kRescaleLog2; u(r)/l(r) does
+            // not depend on r, and with r within kRescaleLog2 of the max every
+            // weight stays <= 2^kRescaleLog2.  r is in log2 units of the scaled score.
+            float r_base = -INFINITY;
+            float l_run = 0.f;
+            for (int j = 0; j < my_nkv; ++j) {
+                ok = wait_or_abort(bar_s_full(t), scnt & 1, p.err, kSiteS, abort_flag);
+                if (!ok) break;
+                ++scnt;
+                // S_t(j) complete implies every MMA issued before it is complete:
+                // the releasing tile (the one active in every KV step) hands K_j
+                // and V_{j-1} back to the producer with a plain arrive.
+                if (t == it.t_rel && quarter == 0 && lane == 0) {
+                    mbar_arrive(bar_kv_empty((g + 2 * j) % C::kSlots));
+                    if (j > 0) mbar_arrive(bar_kv_empty((g + 2 * j - 1) % C::kSlots));
+                }
+                tc_fence_after();
+                __syncwarp();
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+
+                // mask: keys beyond key_len / the sequence, and the causal future
+                const int kbase = j * BN;
+                const bool need_mask = (kbase + BN > klen) || (p.causal && kbase + BN > my_row0);
+                if (need_mask) {
+                    int lim = klen - kbase;
+                    if (p.causal) lim = min(lim, qi - kbase + 1);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
+                }
+                // row max: four independent chains of three-input maxima
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
-            }
-            // row max: four independent chains of three-input maxima
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int e = 0; e < 32; e += 2)
-                    mx[(e >> 1) & 3] = fmax3(mx[(e >> 1) & 3], __uint_as_float(sr[c][e]),
-                                             __uint_as_float(sr[c][e + 1]));
-            const float mrow = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
-            const bool resc = mrow > r_base + kRescaleLog2;   // always true on the first valid tile
-            const float r_new = resc ? mrow : r_base;
-            // a row that has seen no valid key keeps a finite base, so no
-            // -inf - (-inf) appears; its weights are then all zero
-            const float r_use = (r_new == -INFINITY) ? 0.f : r_new;
-            const float alpha = resc ? ex2(r_base - r_use) : 1.f;  // 0 when r_base = -inf
-            const float2 nr2 = make_float2(-r_use, -r_use);
-            const float2 sl22 = make_float2(sl2, sl2);
+                    for (int e = 0; e < 32; e += 2)
+                        mx[(e >> 1) & 3] = fmax3(mx[(e >> 1) & 3], __uint_as_float(sr[c][e]),
+                                                 __uint_as_float(sr[c][e + 1]));
+                const float mrow = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+                const bool resc = mrow > r_base + kRescaleLog2;   // always true on the first valid tile
+                const float r_new = resc ? mrow : r_base;
+                // a row that has seen no valid key keeps a finite base, so no
+                // -inf - (-inf) appears; its weights are then all zero
+                const float r_use = (r_new == -INFINITY) ? 0.f : r_new;
+                const float alpha = resc ? ex2(r_base - r_use) : 1.f;  // 0 when r_base = -inf
+                const float2 nr2 = make_float2(-r_use, -r_use);
+                const float2 sl22 = make_float2(sl2, sl2);
 
-            float2 ls[4];
+                float2 ls[4];
 #pragma unroll
-            for (int a = 0; a < 4; ++a) ls[a] = make_float2(0.f, 0.f);
+                for (int a = 0; a < 4; ++a) ls[a] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float2 x = __ffma2_rn(
-                        make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sl22, nr2);
-                    const float2 w = make_float2(ex2(x.x), ex2(x.y));
-                    ls[(e >> 1) & 3] = __fadd2_rn(ls[(e >> 1) & 3], w);
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(w.x, w.y);
-                    pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&pr);
-                }
-                // P columns 16c .. 16c+15 of this tile's S region
-#pragma unroll
-                for (int e = 0; e < 16; ++e) sr[c][e] = pk[e];
-            }
-            {
-                uint32_t lo[32], hi[32];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    lo[e] = sr[0][e];
-                    lo[16 + e] = sr[1][e];
-                    hi[e] = sr[2][e];
-                    hi[16 + e] = sr[3][e];
-                }
-                tmem_st32(s_addr + 0, lo);
-                tmem_st32(s_addr + 32, hi);
-            }
-            const float2 s01 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
-            l_run = fmaf(l_run, alpha, s01.x + s01.y);
-            r_base = r_new;
-
-            // correction U <- alpha U, only when some row of the warp moved its
-            // base (O holds the complete PV(j-1) at this point)
-            if (j > 0 && __any_sync(0xffffffffu, resc)) {
-                const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-                for (int c = 0; c < D / 32; c += 2) {
-                    uint32_t o0[32], o1[32];
-                    tmem_ld32(o_addr + c * 32, o0);
-                    tmem_ld32(o_addr + (c + 1) * 32, o1);
-                    tmem_wait_ld();
-                    reg_fence(o0);
-                    reg_fence(o1);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        float2 v0 = __fmul2_rn(make_float2(__uint_as_float(o0[e]), __uint_as_float(o0[e + 1])), a2);
-                        float2 v1 = __fmul2_rn(make_float2(__uint_as_float(o1[e]), __uint_as_float(o1[e + 1])), a2);
-                        o0[e] = __float_as_uint(v0.x);
-                        o0[e + 1] = __float_as_uint(v0.y);
-                        o1[e] = __float_as_uint(v1.x);
-                        o1[e + 1] = __float_as_uint(v1.y);
+                        const float2 x = __ffma2_rn(
+                            make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sl22, nr2);
+                        const float2 w = make_float2(ex2(x.x), ex2(x.y));
+                        ls[(e >> 1) & 3] = __fadd2_rn(ls[(e >> 1) & 3], w);
+                        const __nv_bfloat162 pr = __floats2bfloat162_rn(w.x, w.y);
+                        pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&pr);
                     }
-                    tmem_st32(o_addr + c * 32, o0);
-                    tmem_st32(o_addr + (c + 1) * 32, o1);
+                    // P columns 16c .. 16c+15 of this tile's S region
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) sr[c][e] = pk[e];
                 }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_p_ready(t));
-        }
+                {
+                    uint32_t lo[32], hi[32];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        lo[e] = sr[0][e];
+                        lo[16 + e] = sr[1][e];
+                        hi[e] = sr[2][e];
+                        hi[16 + e] = sr[3][e];
+                    }
+                    tmem_st32(s_addr + 0, lo);
+                    tmem_st32(s_addr + 32, hi);
+                }
+                const float2 s01 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
+                l_run = fmaf(l_run, alpha, s01.x + s01.y);
+                r_base = r_new;
 
-        // ---- epilogue: O = U / l, L = m + log l
-        const bool have = ok && my_nkv > 0;
-        if (have) ok = wait_or_abort(bar_o_final(t), 0, p.err, kSiteO, abort_flag);
-        const bool store = qi < N && my_row0 < N;
-        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.O) + (static_cast<size_t>(bh) * N + qi) * D;
-        if (have && ok) {
-            tc_fence_after();
-            __syncwarp();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                // correction U <- alpha U, only when some row of the warp moved its
+                // base (O holds the complete PV(j-1) at this point)
+                if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(o_addr + c * 32, o);
-                tmem_wait_ld();
-                reg_fence(o);
-                if (store) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                    for (int c = 0; c < D / 32; c += 2) {
+                        uint32_t o0[32], o1[32];
+                        tmem_ld32(o_addr + c * 32, o0);
+                        tmem_ld32(o_addr + (c + 1) * 32, o1);
+                        tmem_wait_ld();
+                        reg_fence(o0);
+                        reg_fence(o1);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const __nv_bfloat162 pr = __floats2bfloat162_rn(
-                                __uint_as_float(o[v * 8 + 2 * e]) * inv, __uint_as_float(o[v * 8 + 2 * e + 1]) * inv);
-                            w[e] = *reinterpret_cast<const uint32_t *>(&pr);
+                        for (int e = 0; e < 32; e += 2) {
+                            float2 v0 = __fmul2_rn(make_float2(__uint_as_float(o0[e]), __uint_as_float(o0[e + 1])), a2);
+                            float2 v1 = __fmul2_rn(make_float2(__uint_as_float(o1[e]), __uint_as_float(o1[e + 1])), a2);
+                            o0[e] = __float_as_uint(v0.x);
+                            o0[e + 1] = __float_as_uint(v0.y);
+                            o1[e] = __float_as_uint(v1.x);
+                            o1[e + 1] = __float_as_uint(v1.y);
                         }
-                        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                        tmem_st32(o_addr + c * 32, o0);
+                        tmem_st32(o_addr + (c + 1) * 32, o1);
                     }
                 }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_p_ready(t));
             }
-            if (store && p.L)
-                p.L[static_cast<size_t>(bh) * N + qi] = l_run > 0.f ? (r_base + __log2f(l_run)) * kLn2 : -INFINITY;
-        } else if (!have && store) {
-            // no valid key for this row (key_len = 0): O = 0, L = -inf
-            uint4 *dst = reinterpret_cast<uint4 *>(orow);
-            for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
-            if (p.L) p.L[static_cast<size_t>(bh) * N + qi] = -INFINITY;
+            if (!ok) break;
+
+            // ---- epilogue: O = U / l, L = m + log l
+            if (my_nkv > 0) {
+                ok = wait_or_abort(bar_o_final(t), uses & 1, p.err, kSiteO, abort_flag);
+                if (!ok) break;
+                ++uses;
+                tc_fence_after();
+                __syncwarp();
+                // the last V tile of the item is free once the item's last PV completed
+                if (t == it.t_rel && quarter == 0 && lane == 0)
+                    mbar_arrive(bar_kv_empty((g + 2 * it.ntot - 1) % C::kSlots));
+                uint32_t o[D / 32][32];
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) tmem_ld32(o_addr + c * 32, o[c]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) reg_fence(o[c]);
+                // O_t has been read: the next item's PV_t(0) may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_o_free(t));
+                if (store) {
+                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const __nv_bfloat162 pr =
+                                    __floats2bfloat162_rn(__uint_as_float(o[c][v * 8 + 2 * e]) * inv,
+                                                          __uint_as_float(o[c][v * 8 + 2 * e + 1]) * inv);
+                                w[e] = *reinterpret_cast<const uint32_t *>(&pr);
+                            }
+                            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                    if (p.L)
+                        p.L[static_cast<size_t>(it.bh) * N + qi] =
+                            l_run > 0.f ? (r_base + __log2f(l_run)) * kLn2 : -INFINITY;
+                }
+            } else if (store) {
+                // no valid key for this row (key_len = 0): O = 0, L = -inf
+                uint4 *dst = reinterpret_cast<uint4 *>(orow);
+                for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+                if (p.L) p.L[static_cast<size_t>(it.bh) * N + qi] = -INFINITY;
+            }
+            g += 2 * it.ntot;
         }
     }
 
@@ -557,8 +650,19 @@ cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
     }
     if (!regs_ok) return cudaErrorInvalidConfiguration;
     const int npairs = (p.N + 2 * BM - 1) / (2 * BM);
-    dim3 grid(npairs, p.H, p.B);
-    prefill_kernel<D><<<grid, kThreads, smem, stream>>>(tm, p);
+    const long long items = static_cast<long long>(npairs) * p.H * p.B;
+    if (items > (1ll << 30)) return cudaErrorInvalidValue;
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    // persistent: one CTA per SM (shared memory and TMEM allow no more)
+    const int grid = static_cast<int>(items < sms ? items : sms);
+    prefill_kernel<D><<<grid, kThreads, smem, stream>>>(tm, p, static_cast<int>(items), npairs);
     return cudaGetLastError();
 }
 

@@ -92,6 +92,22 @@ def recorded_traffic(kernel):
     return ent.get("bytes_per_launch")
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(values, device, world):
+    """Element-wise maximum of per-rank timings (identity on one rank)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_throughput(work_per_rank, ms_slowest, world):
+    """Whole-job rate of `world` independent replicas: all ranks' work over the slowest rank's time."""
+    return world * work_per_rank / (ms_slowest * 1e-3)
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -307,17 +323,12 @@ def run_ours(args, rank, world, local_rank):
 
     flops = prefill_flops(wp.B, wp.H, wp.N, wp.d, wp.causal)
     dbytes = decode_bytes(wd.H, seqlens.tolist(), wd.d)
-    pf = statistics.mean(pf_ms)
-    dc = statistics.mean(dc_ms)
-    ee = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([pf, dc, ee], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        pf, dc, ee = t.tolist()
+    pf, dc, ee = max_over_ranks([statistics.mean(pf_ms), statistics.mean(dc_ms), statistics.mean(e2e_ms)],
+                                dev, world)
 
-    tflops = world * flops / (pf * 1e-3) / 1e12
-    gbs = world * dbytes / (dc * 1e-3) / 1e9
-    e2e_tflops = world * flops / (ee * 1e-3) / 1e12
+    tflops = replica_throughput(flops, pf, world) / 1e12
+    gbs = replica_throughput(dbytes, dc, world) / 1e9
+    e2e_tflops = replica_throughput(flops, ee, world) / 1e12
     per_gpu_tflops = flops / (pf * 1e-3) / 1e12
     per_gpu_gbs = dbytes / (dc * 1e-3) / 1e9
     src = peaks["source"]

@@ -67,6 +67,8 @@ def library():
         lib.fa_device_error.argtypes = [_i, ctypes.POINTER(_i)]
         lib.fa_device_error.restype = _i
         lib.fa_version.restype = _i
+        lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
+        lib.fa_selftest_wait_timeout.restype = _i
         _lib = lib
         return lib
 

@@ -193,6 +193,16 @@ fa_status fa_device_error(int clear, int *site) {
     return v ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
 }
 
+fa_status fa_selftest_wait_timeout(unsigned limit_us, fa_stream_t stream) {
+    if (limit_us < 1 || limit_us > 100000) return FA_ERR_INVALID_ARG;
+    unsigned *err = nullptr;
+    fa_status s = error_word(&err);
+    if (s != FA_OK) return s;
+    if (launch_wait_selftest(1000ull * limit_us, err, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
+}
+
 fa_status fa_decode_plan(int B, int H, int Lmax, int d, int num_splits, const int32_t *seqlens_host,
                          int num_sms, int *chunk_len, int *max_chunks) {
     if (!chunk_len || !max_chunks || !decode_shape_ok(B, H, Lmax, d)) return FA_ERR_INVALID_ARG;

@@ -48,4 +48,8 @@ struct PrefillParams {
 
 cudaError_t launch_prefill(const PrefillParams &p, int d, cudaStream_t stream);
 
+// ------------------------------------------------------------------ self-test
+constexpr int kSiteSelfTest = 0x301;
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned *err, cudaStream_t stream);
+
 }  // namespace fa

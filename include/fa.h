@@ -183,6 +183,16 @@ FA_API const char *fa_status_string(fa_status s);
  */
 FA_API fa_status fa_device_error(int clear, int *site);
 
+/*
+ * fa_selftest_wait_timeout -- exercise the bounded-wait failure path.
+ * (No counterpart on the pages: a check of this library's failure handling.)
+ * Launches one thread that waits, for limit_us microseconds (1 .. 100000),
+ * on a barrier nothing arrives at.  The wait gives up, records site 0x301 in
+ * the device error word and returns; the context stays usable.  A following
+ * fa_device_error() returns FA_ERR_DEVICE_TIMEOUT with *site = 0x301.
+ */
+FA_API fa_status fa_selftest_wait_timeout(unsigned limit_us, fa_stream_t stream);
+
 /* Library ABI version (major * 100 + minor). */
 FA_API int fa_version(void);
 

@@ -65,6 +65,7 @@ constexpr int kThreads = 384;        // 3 warpgroups: softmax 0, softmax 1, prod
 constexpr int kRegsSoftmax = 216;    // per-thread registers of the softmax warpgroups after setmaxnreg
 constexpr int kRegsAux = 72;         // per-thread registers of the producer/MMA warpgroup
 constexpr int kTmemCols = 512;
+constexpr long long kL2BlockBytes = 16ll << 20;  // K+V budget of a block of (batch, head) units
 constexpr int kPrefetchTiles = 4;   // L2 prefetch distance of the KV stream, in KV tiles
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleLog2 = 8.0f;  // move the exponent base only when the max grows by > 2^8
@@ -114,12 +115,18 @@ struct Item {
     int row0[2], nkv[2];
 };
 
-__device__ __forceinline__ Item item_info(const PrefillParams &p, int k, int npairs) {
+// Item order: (batch, head) units are taken in blocks of `upb`; inside a
+// block the heaviest causal pairs come first and the block's units share each
+// pair index, so concurrently running CTAs read the same K/V tiles from L2.
+__device__ __forceinline__ Item item_info(const PrefillParams &p, int k, int npairs, int upb) {
     Item it;
     const int units = p.B * p.H;
-    // heaviest causal pairs first, all heads of a pair index together
-    const int pair = npairs - 1 - k / units;
-    it.bh = k % units;
+    const int block = k / (npairs * upb);
+    const int first = block * upb;
+    const int in_block = min(upb, units - first);
+    const int rem = k - block * npairs * upb;
+    const int pair = npairs - 1 - rem / in_block;
+    it.bh = first + rem % in_block;
     it.b = it.bh / p.H;
     it.h = it.bh % p.H;
     const int N = p.N;
@@ -152,7 +159,7 @@ __device__ __forceinline__ int item_of_round(int r, int G, int c) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ TmapSet tm, const PrefillParams p, int num_items, int npairs) {
+    prefill_kernel(const __grid_constant__ TmapSet tm, const PrefillParams p, int num_items, int npairs, int upb) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzled tiles need 1024-byte aligned bases.
@@ -223,12 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int r = 0; ok; ++r) {
                     const int k = item_of_round(r, G, cta);
                     if (k >= num_items) break;
-                    const Item it = item_info(p, k, npairs);
+                    const Item it = item_info(p, k, npairs, upb);
                     if (it.ntot == 0) continue;
                     // Q of the next item of this CTA: warm L2 while this one runs
                     const int kn = item_of_round(r + 1, G, cta);
                     if (kn < num_items) {
-                        const Item nx = item_info(p, kn, npairs);
+                        const Item nx = item_info(p, kn, npairs, upb);
 #pragma unroll
                         for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -316,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int r = 0; ok; ++r) {
                     const int k = item_of_round(r, G, cta);
                     if (k >= num_items) break;
-                    const Item it = item_info(p, k, npairs);
+                    const Item it = item_info(p, k, npairs, upb);
                     if (it.ntot == 0) continue;
                     ok = wait_or_abort(bar_q, qi & 1, p.err, kSiteQ, abort_flag);
                     if (ok) ok = wait_or_abort(bar_kv_full(g % C::kSlots), (g / C::kSlots) & 1, p.err, kSiteKvFull,
@@ -400,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rr = 0; ok; ++rr) {
             const int k = item_of_round(rr, G, cta);
             if (k >= num_items) break;
-            const Item it = item_info(p, k, npairs);
+            const Item it = item_info(p, k, npairs, upb);
             const int my_row0 = t ? it.row0[1] : it.row0[0];
             const int my_nkv = t ? it.nkv[1] : it.nkv[0];
             const int klen = it.klen;
@@ -662,7 +669,17 @@ cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
     }
     // persistent: one CTA per SM (shared memory and TMEM allow no more)
     const int grid = static_cast<int>(items < sms ? items : sms);
-    prefill_kernel<D><<<grid, kThreads, smem, stream>>>(tm, p, static_cast<int>(items), npairs);
+    // (batch, head) units per L2 block.  Non-causal items all cost the same,
+    // so blocks whose K+V take <= kL2BlockBytes keep the concurrently running
+    // CTAs on shared K/V tiles.  Causal items differ up to 64x in cost: there
+    // the whole problem is one block, ordered heaviest first, because the
+    // static schedule balances only a globally sorted order (measured: head
+    // blocks cost more in balance than they gain in L2 hits).
+    const long long kv_unit = 2ll * p.N * D * 2;
+    long long upb = p.causal ? BH : kL2BlockBytes / (kv_unit > 0 ? kv_unit : 1);
+    if (upb < 1) upb = 1;
+    if (upb > static_cast<long long>(BH)) upb = BH;
+    prefill_kernel<D><<<grid, kThreads, smem, stream>>>(tm, p, static_cast<int>(items), npairs, static_cast<int>(upb));
     return cudaGetLastError();
 }
 

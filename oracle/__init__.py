@@ -22,5 +22,6 @@ from .oracle import (  # noqa: F401
     sdpa_rows,
     sdpa_forward,
     decode,
+    decode_paged,
     max_threads,
 )

@@ -287,6 +287,66 @@ int oracle_decode(const uint16_t *q, const uint16_t *Kc, const uint16_t *Vc,
                             (int64_t)B * H, O_out, lse_out, nthreads);
 }
 
+/* Paged decode ("CMU 10-423 Lecture 18", section 7.3, PagedAttention): the
+ * cache is a pool of fixed-size blocks, and block_table[b * max_blocks + i]
+ * names the physical block that holds tokens i*bs .. i*bs+bs-1 of sequence b.
+ * Pool layout: [num_blocks][H][bs][d] (bf16 bits).  The keys and values of
+ * sequence b are gathered through its table (tokens t < seqlens[b], clamped
+ * to max_blocks * bs) and attended exactly as in oracle_decode: one explicit
+ * score row, its stable softmax, no split.  Returns -1 on a table entry
+ * outside [0, num_blocks). */
+int oracle_decode_paged(const uint16_t *q, const uint16_t *Kpool, const uint16_t *Vpool,
+                        const int32_t *block_table, int max_blocks, const int32_t *seqlens,
+                        int B, int H, int num_blocks, int bs, int d, double scale,
+                        double *O_out, double *lse_out, int nthreads)
+{
+    if (B < 0 || H < 0 || num_blocks <= 0 || bs <= 0 || d <= 0 || max_blocks < 0) return -1;
+    if (nthreads <= 0) nthreads = 1;
+    const int cap = max_blocks * bs;
+    int bad = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
+        const int b = (int)(bh / H), h = (int)(bh % H);
+        int n = seqlens[b];
+        if (n < 0) n = 0;
+        if (n > cap) n = cap;
+        double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        double *vr = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)d);
+        double *qv = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!s || !vr || !qv) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            bad = 1;
+            free(s); free(vr); free(qv);
+            continue;
+        }
+        for (int c = 0; c < d; ++c) qv[c] = widen_bf16(q[(size_t)bh * d + c]);
+        int ok = 1;
+        for (int t = 0; t < n && ok; ++t) {
+            const int phys = block_table[(size_t)b * max_blocks + t / bs];
+            if (phys < 0 || phys >= num_blocks) { ok = 0; break; }
+            const size_t row = (((size_t)phys * H + h) * bs + (size_t)(t % bs)) * d;
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) acc += qv[c] * widen_bf16(Kpool[row + c]);
+            s[t] = scale * acc;
+            for (int c = 0; c < d; ++c) vr[(size_t)t * d + c] = widen_bf16(Vpool[row + c]);
+        }
+        if (ok) {
+            oracle_attend_scores(s, vr, n, d, O_out + (size_t)bh * d, lse_out + bh);
+        } else {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            bad = 1;
+        }
+        free(s); free(vr); free(qv);
+    }
+    return bad ? -1 : 0;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

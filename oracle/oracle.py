@@ -79,6 +79,10 @@ def _load():
                                       ctypes.c_int, ctypes.c_int, ctypes.c_double, _dp, _dp,
                                       ctypes.c_int]
         lib.oracle_decode.restype = ctypes.c_int
+        lib.oracle_decode_paged.argtypes = [_u16p, _u16p, _u16p, _i32p, ctypes.c_int, _i32p, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_double, _dp, _dp, ctypes.c_int]
+        lib.oracle_decode_paged.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -289,3 +293,34 @@ def decode(q, Kc, Vc, seqlens, scale=None, nthreads=None):
     if rc != 0:
         raise ValueError("oracle_decode rejected its arguments")
     return O, L
+
+
+def decode_paged(q, Kpool, Vpool, block_table, seqlens, scale=None, nthreads=None):
+    """Single-query attention through a block table (no split).
+
+    q: [B, H, d]; Kpool, Vpool: [num_blocks, H, block_size, d];
+    block_table: int32 [B, max_blocks].  Returns O [B, H, d], L [B, H].
+    """
+    B, H, d = tuple(q.shape)
+    nblk, H2, bs, d2 = tuple(Kpool.shape)
+    if H2 != H or d2 != d:
+        raise ValueError("pool must be [num_blocks, H, block_size, d]")
+    qb = _bf16_bits(q)
+    kb = _bf16_bits(Kpool)
+    vb = _bf16_bits(Vpool)
+    bt = _i32(block_table)
+    if bt.ndim != 2 or bt.shape[0] != B:
+        raise ValueError("block_table must be [B, max_blocks]")
+    sl = _i32(seqlens)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    O = np.empty((B, H, d))
+    L = np.empty((B, H))
+    rc = _load().oracle_decode_paged(_ptr(qb, _u16p), _ptr(kb, _u16p), _ptr(vb, _u16p),
+                                     _ptr(np.ascontiguousarray(bt), _i32p), bt.shape[1],
+                                     _ptr(sl, _i32p), B, H, nblk, bs, d, float(scale),
+                                     _ptr(O, _dp), _ptr(L, _dp), _threads(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_decode_paged rejected its arguments (table entry out of range?)")
+    return O, L
+

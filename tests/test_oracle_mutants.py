@@ -33,6 +33,10 @@ MUTANTS = {
                                  "double w = l_k[k] / l_f;"),
     "bf16_widen_wrong_half": ("uint32_t word = ((uint32_t)bits) << 16;",
                               "uint32_t word = ((uint32_t)bits) << 15;"),
+    "paged_row_in_block": ("const size_t row = (((size_t)phys * H + h) * bs + (size_t)(t % bs)) * d;",
+                           "const size_t row = (((size_t)phys * H + h) * bs + (size_t)(t / bs)) * d;"),
+    "paged_head_ignored": ("const size_t row = (((size_t)phys * H + h) * bs + (size_t)(t % bs)) * d;",
+                           "const size_t row = (((size_t)phys * H + 0) * bs + (size_t)(t % bs)) * d;"),
 }
 
 

@@ -387,3 +387,63 @@ def test_causal_tile_count_closed_form():
     tiles = sum(1 for i in range(T) for j in range(T) if j <= i)
     assert tiles == g["tiles"]
     assert tiles * g["ratio_den"] == T * T * g["ratio_num"]
+
+
+# ---------------------------------------------------------------- paged decode
+
+def _pool_from_contiguous(Kc, table, bs, nblk):
+    """Scatter a contiguous cache [B, H, L, d] into a pool [nblk, H, bs, d] via table."""
+    B, H, L, d = Kc.shape
+    pool = torch.full((nblk, H, bs, d), 7.0, dtype=torch.bfloat16)   # junk everywhere else
+    for b in range(B):
+        for i in range(table.shape[1]):
+            lo = i * bs
+            if lo >= L:
+                break
+            n = min(bs, L - lo)
+            pool[table[b, i], :, :n] = Kc[b, :, lo:lo + n]
+    return pool
+
+
+def test_paged_decode_lecture_example_matches_contiguous():
+    """Lecture 18 section 7.3: 12 physical blocks of 4 tokens; request B's table is 1 -> 4 -> 5.
+    Keys fetched through the table are the request's own; attention equals the contiguous one."""
+    H, d, bs, nblk = 2, 8, 4, 12
+    q = _bf16((1, H, d), 50)
+    Kc = _bf16((1, H, 12, d), 51)
+    Vc = _bf16((1, H, 12, d), 52)
+    table = torch.tensor([[1, 4, 5]], dtype=torch.int32)
+    Kp = _pool_from_contiguous(Kc, table, bs, nblk)
+    Vp = _pool_from_contiguous(Vc, table, bs, nblk)
+    for n in (12, 10, 5, 1):     # a partly filled last block wastes at most bs - 1 slots
+        Op, Lp = oracle.decode_paged(q, Kp, Vp, table, [n])
+        Oc, Lc = oracle.decode(q, Kc, Vc, [n])
+        np.testing.assert_array_equal(Op, Oc)
+        np.testing.assert_array_equal(Lp, Lc)
+
+
+def test_paged_decode_scrambled_pool_and_unused_slots():
+    B, H, d, bs, L = 3, 2, 16, 16, 80
+    nblk = 3 * (L // bs) + 4
+    q = _bf16((B, H, d), 60)
+    Kc = _bf16((B, H, L, d), 61)
+    Vc = _bf16((B, H, L, d), 62)
+    perm = torch.randperm(nblk, generator=torch.Generator().manual_seed(6))[:B * (L // bs)]
+    table = perm.reshape(B, L // bs).to(torch.int32)
+    Kp = _pool_from_contiguous(Kc, table, bs, nblk)
+    Vp = _pool_from_contiguous(Vc, table, bs, nblk)
+    seqlens = [80, 33, 1]
+    Op, Lp = oracle.decode_paged(q, Kp, Vp, table, seqlens)
+    Oc, Lc = oracle.decode(q, Kc, Vc, seqlens)
+    np.testing.assert_array_equal(Op, Oc)
+    np.testing.assert_array_equal(Lp, Lc)
+    # brute force on one row
+    Oe, Le = _mp_attention(q[1:2, :, None, :], Kc[1:2, :, :33], Vc[1:2, :, :33], False,
+                           1.0 / math.sqrt(d), None)
+    np.testing.assert_allclose(Op[1], Oe[0, :, 0], atol=1e-14)
+    np.testing.assert_allclose(Lp[1], Le[0, :, 0], atol=1e-14)
+    # an out-of-range table entry is rejected
+    bad = table.clone()
+    bad[0, 0] = nblk
+    with pytest.raises(ValueError):
+        oracle.decode_paged(q, Kp, Vp, bad, seqlens)

@@ -298,6 +298,23 @@ def run_ours(args, rank, world, local_rank):
                                            "frac_of_hbm_peak": round(by5 / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                                            "chunk_len": c5, "max_chunks": n5}
     del q5, K5, V5
+    # paged cache: the decode workload's shape held in scattered blocks of a pool
+    for bs in (16, 64):
+        qp, Kp, Vp, tbl, slp = workloads.paged_inputs(wd.B, wd.H, bs, wd.d, seqlens, wd.seed, device=dev)
+        tbld, slpd = tbl.to(dev), slp.to(dev)
+        wsp = torch.empty(fa.fa_decode_workspace_bytes(wd.B, wd.H, tbl.shape[1] * bs, wd.d, 0, slp), device=dev,
+                          dtype=torch.uint8)
+        ms = timed(lambda: fa.fa_decode_paged(qp, Kp, Vp, tbld, slpd, num_splits=0, seqlens_host=slp,
+                                              workspace=wsp))
+        byp = decode_bytes(wd.H, slp.tolist(), wd.d)
+        others[f"decode_paged_b1h32_l32768_d128_bs{bs}"] = {
+            "ms": round(ms, 4), "bytes": byp, "gbs": round(byp / (ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm_peak": round(byp / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "block_size": bs, "num_blocks": int(Kp.shape[0])}
+        del qp, Kp, Vp
+    st, site = fa.fa_device_error(clear=True)
+    if st != 0:
+        raise RuntimeError(f"device error word set by the other workloads (site {site:#x})")
 
     # ---- end to end through the public call with host buffers
     Qh, Kh, Vh = (t.cpu().pin_memory() for t in (Q, K, V))

@@ -8,6 +8,7 @@ PyTorch fallback, and the calls raise if ``libfa.so`` is missing.
 
     fa_forward(Q, K, V, causal=False, scale=None, key_len=None) -> (O, L)
     fa_decode(q, Kcache, Vcache, seqlens, num_splits=0, ...)   -> (O, L)
+    fa_decode_paged(q, Kpool, Vpool, block_table, seqlens, ...) -> (O, L)
 """
 from __future__ import annotations
 
@@ -15,7 +16,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["fa_forward", "fa_decode", "fa_decode_plan", "fa_decode_workspace_bytes",
+__all__ = ["fa_forward", "fa_decode", "fa_decode_paged", "fa_decode_plan", "fa_decode_workspace_bytes",
            "fa_device_error", "FaError", "library", "library_path", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -55,6 +56,9 @@ def library():
         lib.fa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float, _i,
                                   _vp, ctypes.c_size_t, _vp]
         lib.fa_decode.restype = _i
+        lib.fa_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                         ctypes.c_float, _i, _vp, ctypes.c_size_t, _vp]
+        lib.fa_decode_paged.restype = _i
         lib.fa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float,
                                           _i, _vp]
         lib.fa_decode_noalloc.restype = _i
@@ -192,6 +196,50 @@ def fa_decode(q, Kcache, Vcache, seqlens, num_splits=0, scale=None, seqlens_host
     del keep
     if st != 0:
         raise FaError(st, "fa_decode")
+    return out, lse
+
+
+def fa_decode_paged(q, Kpool, Vpool, block_table, seqlens, num_splits=0, scale=None, seqlens_host=None,
+                    out=None, lse=None, return_lse=True, workspace=None, stream=None):
+    """Split-KV decode over a paged cache.  q: [B, H, d]; pools [num_blocks, H, block_size, d].
+
+    block_table: CUDA int32 [B, max_blocks]; token t of sequence b is row
+    t % block_size of pool block block_table[b, t // block_size].
+    Returns (O [B, H, d] bf16, L [B, H] float32).
+    """
+    torch = _torch()
+    _check_bf16("q", q, 3)
+    _check_bf16("Kpool", Kpool, 4)
+    _check_bf16("Vpool", Vpool, 4)
+    num_blocks, H, bs, d = Kpool.shape
+    B = q.shape[0]
+    if Vpool.shape != Kpool.shape or tuple(q.shape) != (B, H, d):
+        raise ValueError("q must be [B, H, d] and the pools [num_blocks, H, block_size, d]")
+    if (block_table.dtype != torch.int32 or not block_table.is_cuda or block_table.dim() != 2
+            or block_table.shape[0] != B):
+        raise TypeError("block_table must be a CUDA int32 tensor [B, max_blocks]")
+    block_table = block_table.contiguous()
+    max_blocks = block_table.shape[1]
+    if seqlens.dtype != torch.int32 or not seqlens.is_cuda or seqlens.numel() != B:
+        raise TypeError("seqlens must be a CUDA int32 tensor with B entries")
+    seqlens = seqlens.contiguous()
+    if seqlens_host is None:
+        seqlens_host = seqlens.cpu()
+    hp, keep = _host_i32(seqlens_host)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), device=q.device, dtype=torch.float32)
+    need = library().fa_decode_workspace_bytes(B, H, max_blocks * bs, d, num_splits, hp)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    st = library().fa_decode_paged(_ptr(q), _ptr(Kpool), _ptr(Vpool), _ptr(block_table), max_blocks,
+                                   _ptr(seqlens), hp, _ptr(out), _ptr(lse), B, H, num_blocks, bs, d,
+                                   float(scale) if scale is not None else 0.0, int(num_splits),
+                                   _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    del keep
+    if st != 0:
+        raise FaError(st, "fa_decode_paged")
     return out, lse
 
 

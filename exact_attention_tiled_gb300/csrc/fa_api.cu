@@ -189,8 +189,9 @@ fa_status fa_device_error(int clear, int *site) {
         const unsigned zero = 0;
         if (cudaMemcpy(ptr, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
     }
-    if (site) *site = static_cast<int>(v & 0x7FFFFFFFu);
-    return v ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+    if (site) *site = static_cast<int>(v & 0x3FFFFFFFu);
+    if (!v) return FA_OK;
+    return (v & 0x40000000u) ? FA_ERR_INVALID_ARG : FA_ERR_DEVICE_TIMEOUT;
 }
 
 fa_status fa_selftest_wait_timeout(unsigned limit_us, fa_stream_t stream) {
@@ -235,10 +236,22 @@ size_t fa_decode_workspace_bytes(int B, int H, int Lmax, int d, int num_splits,
     return workspace_for(B, H, smax, d);
 }
 
-fa_status fa_decode(const void *q, const void *Kcache, const void *Vcache, const int32_t *seqlens,
-                    const int32_t *seqlens_host, void *O, float *L, int B, int H, int Lmax, int d,
-                    float scale, int num_splits, void *workspace, size_t workspace_bytes,
-                    fa_stream_t stream) {
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+// Shared body of fa_decode and fa_decode_paged: `paged` carries the block
+// table (nullptr for a contiguous cache), in which case Lmax = max_blocks * bs.
+struct PagedArgs {
+    const int32_t *block_table;
+    int block_size, max_blocks, num_blocks;
+};
+
+fa_status decode_impl(const void *q, const void *Kcache, const void *Vcache, const int32_t *seqlens,
+                      const int32_t *seqlens_host, void *O, float *L, int B, int H, int Lmax, int d,
+                      float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                      const PagedArgs &paged, cudaStream_t stream) {
     if (!q || !Kcache || !Vcache || !seqlens || !O) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || Lmax < 1 || B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
@@ -279,8 +292,40 @@ fa_status fa_decode(const void *q, const void *Kcache, const void *Vcache, const
     p.smax = smax;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = err;
-    if (launch_decode(p, d, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    p.block_table = paged.block_table;
+    p.block_size = paged.block_size;
+    p.max_blocks = paged.max_blocks;
+    p.num_blocks = paged.num_blocks;
+    if (launch_decode(p, d, stream) != cudaSuccess) return FA_ERR_CUDA;
     return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_decode(const void *q, const void *Kcache, const void *Vcache, const int32_t *seqlens,
+                    const int32_t *seqlens_host, void *O, float *L, int B, int H, int Lmax, int d,
+                    float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                    fa_stream_t stream) {
+    const PagedArgs contiguous = {nullptr, 0, 0, 0};
+    return decode_impl(q, Kcache, Vcache, seqlens, seqlens_host, O, L, B, H, Lmax, d, scale, num_splits,
+                       workspace, workspace_bytes, contiguous, static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_decode_paged(const void *q, const void *Kpool, const void *Vpool, const int32_t *block_table,
+                          int max_blocks, const int32_t *seqlens, const int32_t *seqlens_host, void *O,
+                          float *L, int B, int H, int num_blocks, int block_size, int d, float scale,
+                          int num_splits, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+    if (!block_table || !aligned(block_table, 4)) return FA_ERR_INVALID_ARG;
+    if (max_blocks < 1 || num_blocks < 1 || block_size < 1 || block_size > FA_PAGED_MAX_BLOCK_SIZE)
+        return FA_ERR_INVALID_ARG;
+    const long long cap = static_cast<long long>(max_blocks) * block_size;
+    if (cap > (1ll << 30)) return FA_ERR_UNSUPPORTED;
+    const PagedArgs paged = {block_table, block_size, max_blocks, num_blocks};
+    return decode_impl(q, Kpool, Vpool, seqlens, seqlens_host, O, L, B, H, static_cast<int>(cap), d, scale,
+                       num_splits, workspace, workspace_bytes, paged, static_cast<cudaStream_t>(stream));
 }
 
 fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *L, int B, int H,

@@ -33,8 +33,9 @@ constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMergeThreads = 256;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// Error-word sites of the bounded waits in this file.
-enum { kSiteDecodeFull = 0x101, kSiteDecodeEmpty = 0x102, kSiteDecodeDrain = 0x103 };
+// Error-word sites in this file.
+enum { kSiteDecodeFull = 0x101, kSiteDecodeEmpty = 0x102, kSiteDecodeDrain = 0x103, kSiteDecodeTable = 0x104 };
+constexpr int kTableWin = 256;       // block-table entries staged in shared memory (paged cache)
 
 __device__ __forceinline__ int clamp_len(int len, int lmax) {
     return len < 0 ? 0 : (len > lmax ? lmax : len);
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(kSplitThreads) decode_split_kernel(const Decod
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + 2 * kStages * kTileBytes);
     uint64_t *empty = full + kStages;
     State *xwarp = reinterpret_cast<State *>(empty + kStages);  // [kConsumerWarps][LPT]
+    int *tbl = reinterpret_cast<int *>(xwarp + kConsumerWarps * LPT);  // [kTableWin] (paged cache)
 
     const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int len = clamp_len(p.seqlens[b], p.Lmax);
@@ -136,31 +138,77 @@ __global__ void __launch_bounds__(kSplitThreads) decode_split_kernel(const Decod
     __syncthreads();
 
     if (warp == kConsumerWarps) {
-        // ------------------------------------------------ producer (one lane)
-        if (lane == 0) {
-            const uint8_t *kbase = static_cast<const uint8_t *>(p.K) + (bh * p.Lmax + t0) * kRowBytes;
-            const uint8_t *vbase = static_cast<const uint8_t *>(p.V) + (bh * p.Lmax + t0) * kRowBytes;
-            const uint64_t pol = l2_policy_evict_first();
-            int issued = 0;
-            bool ok = true;
-            for (int i = 0; i < ntiles; ++i) {
-                const int s = i % kStages;
-                if (i >= kStages) {
-                    ok = mbar_wait(smem_u32(&empty[s]), ((i / kStages) - 1) & 1, p.err,
-                                   kSiteDecodeEmpty);
-                    if (!ok) break;
+        // ------------------------------------------------ producer warp
+        // Lane 0 issues the copies.  With a paged cache the whole warp first
+        // stages a window of the sequence's block table in shared memory; a
+        // tile then takes one bulk copy per physical block it touches
+        // (CMU 10-423 Lecture 18, section 7.3: blocks found through the table).
+        const uint64_t pol = l2_policy_evict_first();
+        const size_t row0 = p.block_table ? 0 : bh * p.Lmax + t0;  // contiguous cache only
+        const uint8_t *kbase = static_cast<const uint8_t *>(p.K) + row0 * kRowBytes;
+        const uint8_t *vbase = static_cast<const uint8_t *>(p.V) + row0 * kRowBytes;
+        int issued = 0;
+        bool ok = true;
+        int win0 = -1;  // first logical block held in tbl
+        for (int i = 0; i < ntiles && ok; ++i) {
+            const int rows = min(kDecodeTile, t1 - t0 - i * kDecodeTile);
+            const int tok0 = t0 + i * kDecodeTile;
+            if (p.block_table) {
+                const int blo = tok0 / p.block_size, bhi = (tok0 + rows - 1) / p.block_size;
+                if (win0 < 0 || bhi >= win0 + kTableWin) {
+                    __syncwarp();
+                    win0 = blo;
+                    const int last = (t1 - 1) / p.block_size;  // last block of this chunk (< max_blocks)
+                    for (int e = lane; e < kTableWin; e += 32) {
+                        const int lb = win0 + e;
+                        int phys = 0;
+                        if (lb <= last) {
+                            phys = p.block_table[static_cast<size_t>(b) * p.max_blocks + lb];
+                            if (phys < 0 || phys >= p.num_blocks) {
+                                report_invalid(p.err, kSiteDecodeTable);
+                                phys = 0;   // never dereference an entry outside the pool
+                            }
+                        }
+                        tbl[e] = phys;
+                    }
+                    __syncwarp();
                 }
-                const int rows = min(kDecodeTile, t1 - t0 - i * kDecodeTile);
-                const uint32_t bytes = static_cast<uint32_t>(rows) * kRowBytes;
-                mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * bytes);
-                bulk_g2s(smem_u32(k_stage + s * kTileBytes), kbase + static_cast<size_t>(i) * kTileBytes,
-                         bytes, smem_u32(&full[s]), pol);
-                bulk_g2s(smem_u32(v_stage + s * kTileBytes), vbase + static_cast<size_t>(i) * kTileBytes,
-                         bytes, smem_u32(&full[s]), pol);
-                ++issued;
             }
-            // Never leave the CTA with copies in flight: wait (bounded) for the
-            // last copies issued into each stage.
+            if (lane == 0) {
+                const int s = i % kStages;
+                if (i >= kStages)
+                    ok = mbar_wait(smem_u32(&empty[s]), ((i / kStages) - 1) & 1, p.err, kSiteDecodeEmpty);
+                if (ok) {
+                    const uint32_t bytes = static_cast<uint32_t>(rows) * kRowBytes;
+                    mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * bytes);
+                    if (!p.block_table) {
+                        bulk_g2s(smem_u32(k_stage + s * kTileBytes), kbase + static_cast<size_t>(i) * kTileBytes,
+                                 bytes, smem_u32(&full[s]), pol);
+                        bulk_g2s(smem_u32(v_stage + s * kTileBytes), vbase + static_cast<size_t>(i) * kTileBytes,
+                                 bytes, smem_u32(&full[s]), pol);
+                    } else {
+                        for (int r = 0; r < rows;) {
+                            const int tok = tok0 + r;
+                            const int lb = tok / p.block_size, rin = tok % p.block_size;
+                            const int n = min(rows - r, p.block_size - rin);
+                            const int phys = tbl[lb - win0];
+                            const size_t src = ((static_cast<size_t>(phys) * p.H + h) * p.block_size + rin) * kRowBytes;
+                            const uint32_t nb = static_cast<uint32_t>(n) * kRowBytes;
+                            bulk_g2s(smem_u32(k_stage + s * kTileBytes + r * kRowBytes),
+                                     static_cast<const uint8_t *>(p.K) + src, nb, smem_u32(&full[s]), pol);
+                            bulk_g2s(smem_u32(v_stage + s * kTileBytes + r * kRowBytes),
+                                     static_cast<const uint8_t *>(p.V) + src, nb, smem_u32(&full[s]), pol);
+                            r += n;
+                        }
+                    }
+                    ++issued;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+        // Never leave the CTA with copies in flight: wait (bounded) for the
+        // last copies issued into each stage.
+        if (lane == 0) {
             const int first = issued > kStages ? issued - kStages : 0;
             for (int i = first; i < issued; ++i)
                 mbar_wait(smem_u32(&full[i % kStages]), (i / kStages) & 1, p.err, kSiteDecodeDrain);
@@ -334,7 +382,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
 template <int D>
 constexpr size_t split_smem_bytes() {
     return 2 * kStages * kDecodeTile * D * 2 + 2 * kStages * sizeof(uint64_t) +
-           kConsumerWarps * (D / 8) * sizeof(State);
+           kConsumerWarps * (D / 8) * sizeof(State) + kTableWin * sizeof(int);
 }
 
 template <int D>

@@ -24,6 +24,10 @@ struct DecodeParams {
     int smax;               // partial slots per (b, h)
     float scale_log2;       // scale * log2(e)
     unsigned *err;          // device error word
+    // paged cache (block_table != nullptr): K and V are pools [num_blocks, H, block_size, d]
+    // and token t of sequence b lives in block block_table[b * max_blocks + t / block_size]
+    const int32_t *block_table;
+    int block_size, max_blocks, num_blocks;
 };
 
 constexpr int kDecodeTile = 64;      // tokens per staged tile

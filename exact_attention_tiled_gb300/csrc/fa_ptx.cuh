@@ -27,6 +27,14 @@ __device__ __forceinline__ void report_timeout(unsigned *err, int site) {
     if (err) atomicCAS(err, 0u, kErrTimeoutBit | (unsigned)site);
 }
 
+// Invalid data found on the device (e.g. a block-table entry outside the
+// pool): recorded as 0x40000000 | site; the kernel substitutes an in-bounds
+// value and carries on, so the outputs of that call are undefined.
+constexpr unsigned kErrInvalidBit = 0x40000000u;
+__device__ __forceinline__ void report_invalid(unsigned *err, int site) {
+    if (err) atomicCAS(err, 0u, kErrInvalidBit | (unsigned)site);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -109,6 +109,87 @@ def decode_inputs(B, H, Lmax, d, seed, amp=1.0, device="cpu"):
     return q, caches[0], caches[1]
 
 
+def paged_inputs(B, H, bs, d, seqlens, seed, spare_blocks=0, amp=1.0, device="cpu"):
+    """Inputs of a paged-cache decode: (q, Kpool, Vpool, block_table, seqlens).
+
+    q is bf16 [B, H, d]; the pools are bf16 [num_blocks, H, bs, d] with
+    num_blocks = sum_b ceil(seqlens[b] / bs) + spare_blocks.  Sequence b
+    owns ceil(seqlens[b] / bs) physical blocks taken from a seeded random
+    permutation of the pool, so logically adjacent blocks are scattered;
+    block_table is int32 [B, max_blocks] (max_blocks = the largest block
+    count, at least 1) with -1 in the slots a sequence does not use.  The
+    table and seqlens are CPU tensors; q and the pools live on `device`.
+    """
+    seqlens = torch.as_tensor(seqlens, dtype=torch.int32).cpu()
+    nblk = [(int(n) + bs - 1) // bs for n in seqlens.tolist()]
+    max_blocks = max(1, max(nblk))
+    num_blocks = max(1, sum(nblk) + int(spare_blocks))
+    g = _gen(device, seed)
+    q = torch.randn((B, H, d), generator=g, device=device, dtype=torch.float32)
+    if amp != 1.0:
+        q = q * amp
+    q = q.to(torch.bfloat16)
+    pools = []
+    step = max(1, (1 << 26) // (H * bs * d))   # blocks drawn per batch, bounds the fp32 temporary
+    for _ in range(2):
+        pool = torch.empty((num_blocks, H, bs, d), device=device, dtype=torch.bfloat16)
+        for b0 in range(0, num_blocks, step):
+            b1 = min(num_blocks, b0 + step)
+            x = torch.randn((b1 - b0, H, bs, d), generator=g, device=device, dtype=torch.float32)
+            if amp != 1.0:
+                x = x * amp
+            pool[b0:b1].copy_(x)
+            del x
+        pools.append(pool)
+    perm = torch.randperm(num_blocks, generator=_gen("cpu", seed + 1)).to(torch.int32)
+    table = torch.full((B, max_blocks), -1, dtype=torch.int32)
+    pos = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[pos:pos + n]
+        pos += n
+    return q, pools[0], pools[1], table, seqlens
+
+
+def shared_prompt_inputs(n_samples, prompt_len, gen_len, bs, H, d, seed, device="cpu"):
+    """Paged inputs of parallel sampling: n_samples answers of gen_len tokens to one prompt.
+
+    The prompt's full blocks are stored once and every answer's block table
+    points at them; the prompt's last, partly filled block is copied on
+    write (each answer but the last gets its own copy holding the same
+    prompt rows, the last answer writes into the original).  Returns
+    (q, Kpool, Vpool, block_table, seqlens) like paged_inputs, with the
+    physical block ids permuted; the pool has
+    prompt_len // bs + n_samples * (ceil((prompt_len + gen_len) / bs) - prompt_len // bs)
+    blocks.
+    """
+    full = prompt_len // bs
+    tail = prompt_len % bs
+    total = prompt_len + gen_len
+    per_seq = (total + bs - 1) // bs
+    own = per_seq - full
+    num_blocks = full + n_samples * own
+    g = _gen(device, seed)
+    q = torch.randn((n_samples, H, d), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    perm = torch.randperm(num_blocks, generator=_gen("cpu", seed + 1))
+    pools = []
+    for _ in range(2):
+        logical = torch.randn((num_blocks, H, bs, d), generator=g, device=device,
+                              dtype=torch.float32).to(torch.bfloat16)
+        if tail:
+            orig = full + (n_samples - 1) * own       # the last answer keeps the original tail block
+            for i in range(n_samples - 1):
+                logical[full + i * own, :, :tail] = logical[orig, :, :tail]
+        pool = torch.empty_like(logical)
+        pool[perm.to(device)] = logical
+        pools.append(pool)
+    table = torch.empty((n_samples, per_seq), dtype=torch.int32)
+    for i in range(n_samples):
+        ids = list(range(full)) + [full + i * own + k for k in range(own)]
+        table[i] = perm[torch.tensor(ids)].to(torch.int32)
+    seqlens = torch.full((n_samples,), total, dtype=torch.int32)
+    return q, pools[0], pools[1], table, seqlens
+
+
 def make(name, device="cpu"):
     """All inputs of a named workload as a dict."""
     w = WORKLOADS[name]

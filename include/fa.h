@@ -172,14 +172,56 @@ FA_API fa_status fa_decode_noalloc(const void *q, const void *Kcache, const void
                                    int B, int H, int Lmax, int d, float scale, int num_splits,
                                    fa_stream_t stream);
 
+/*
+ * fa_decode_paged -- fa_decode over a paged KV cache ("CMU 10-423 Lecture 18",
+ * section 7 "Efficient decoding I: PagedAttention": the cache is a pool of
+ * fixed-size blocks and each sequence reaches its blocks through a block
+ * table, so logically consecutive tokens need not be adjacent in memory).
+ * The attention computed is exactly fa_decode's over the gathered keys and
+ * values; only the addressing differs.
+ *
+ *   Kpool,Vpool   bf16 [num_blocks, H, block_size, d]: row r of head h in
+ *                 physical block p holds one token's key (value).
+ *   block_table   DEVICE int32 [B, max_blocks]: token t of sequence b lives
+ *                 in physical block block_table[b * max_blocks + t / block_size]
+ *                 at row t % block_size.  Only the entries of blocks that
+ *                 hold attended tokens are read; the rest may hold anything.
+ *   max_blocks    table row length, >= 1; max_blocks * block_size <= 2^30.
+ *   seqlens       DEVICE int32 [B], clamped to [0, max_blocks * block_size];
+ *                 seqlens_host as in fa_decode.
+ *   num_blocks    pool size in blocks, >= 1.
+ *   block_size    tokens per block, 1 .. FA_PAGED_MAX_BLOCK_SIZE.  Any value
+ *                 is exact; a multiple of 16 keeps each copy >= 2 KB.
+ *   O, L, d, scale, num_splits, workspace, stream: as in fa_decode; the
+ *                 workspace size is fa_decode_workspace_bytes(B, H,
+ *                 max_blocks * block_size, d, num_splits, seqlens_host).
+ *
+ * A table entry read on the device that lies outside [0, num_blocks) is
+ * never dereferenced: block 0 is read in its place and the device error
+ * word records it, so a following fa_device_error() returns
+ * FA_ERR_INVALID_ARG with *site = 0x104; the outputs of that call are
+ * undefined.
+ */
+#define FA_PAGED_MAX_BLOCK_SIZE 65536
+
+FA_API fa_status fa_decode_paged(const void *q, const void *Kpool, const void *Vpool,
+                                 const int32_t *block_table, int max_blocks,
+                                 const int32_t *seqlens, const int32_t *seqlens_host,
+                                 void *O, float *L,
+                                 int B, int H, int num_blocks, int block_size, int d,
+                                 float scale, int num_splits,
+                                 void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 FA_API const char *fa_status_string(fa_status s);
 
 /*
- * Device-side error word of the current device: 0 when no bounded wait has
- * run out since the last clear, otherwise FA_ERR_DEVICE_TIMEOUT with the
- * wait site in *site (may be NULL).  Synchronises the device.  clear != 0
- * resets the word.
+ * Device-side error word of the current device: FA_OK when nothing has
+ * been recorded since the last clear; FA_ERR_DEVICE_TIMEOUT when a bounded
+ * wait ran out; FA_ERR_INVALID_ARG when a kernel met invalid device data
+ * (a paged-cache table entry outside the pool).  The first event recorded
+ * wins; its site goes to *site (may be NULL).  Synchronises the device.
+ * clear != 0 resets the word.
  */
 FA_API fa_status fa_device_error(int clear, int *site);
 

@@ -155,3 +155,42 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fa, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         fa.library()
+
+
+def _paged(lib, **kw):
+    a = dict(q=FAKE, K=FAKE, V=FAKE, bt=FAKE, mb=8, sl=FAKE, slh=None, O=FAKE, L=None, B=2, H=2, nb=16,
+             bs=16, d=128, scale=0.0, splits=4, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    return lib.fa_decode_paged(a["q"], a["K"], a["V"], a["bt"], a["mb"], a["sl"], a["slh"], a["O"], a["L"],
+                               a["B"], a["H"], a["nb"], a["bs"], a["d"], ctypes.c_float(a["scale"]),
+                               a["splits"], a["ws"], a["wsb"], None)
+
+
+def test_paged_decode_rejects_bad_arguments_before_cuda(lib):
+    assert _paged(lib, bt=None) == 1
+    assert _paged(lib, bt=FAKE + 2) == 1       # table must be 4-byte aligned
+    assert _paged(lib, mb=0) == 1
+    assert _paged(lib, nb=0) == 1
+    assert _paged(lib, bs=0) == 1
+    assert _paged(lib, bs=65537) == 1
+    assert _paged(lib, mb=1 << 20, bs=4096) == 2   # more than 2^30 tokens per sequence
+    assert _paged(lib, K=FAKE + 8) == 1
+    assert _paged(lib, d=96) == 2
+    assert _paged(lib, ws=None) == 4
+    assert _paged(lib, ws=FAKE + 16) == 4
+
+
+def test_paged_inputs_structure():
+    from exact_attention_tiled_gb300 import workloads
+    lens = [100, 0, 16, 33]
+    q, Kp, Vp, table, sl = workloads.paged_inputs(4, 2, 16, 64, lens, seed=3, spare_blocks=4)
+    need = [7, 0, 1, 3]
+    assert tuple(Kp.shape) == (sum(need) + 4, 2, 16, 64) and Vp.shape == Kp.shape
+    assert tuple(table.shape) == (4, 7) and table.dtype.is_signed
+    used = []
+    for b, n in enumerate(need):
+        assert (table[b, n:] == -1).all()
+        used += table[b, :n].tolist()
+    assert len(set(used)) == len(used) and all(0 <= u < Kp.shape[0] for u in used)
+    assert used != sorted(used)                # blocks are scattered, not in logical order
+    assert sl.tolist() == lens

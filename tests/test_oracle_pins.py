@@ -447,3 +447,25 @@ def test_paged_decode_scrambled_pool_and_unused_slots():
     bad[0, 0] = nblk
     with pytest.raises(ValueError):
         oracle.decode_paged(q, Kp, Vp, bad, seqlens)
+
+
+def test_paged_decode_shared_prompt_blocks():
+    """Lecture 18 section 7.5: one 200-token prompt, 4 answers of 100 tokens, blocks of 16.
+    Without sharing the answers take 76 blocks, sharing the prompt takes 40; the prompt's
+    last block (200 is not a multiple of 16) is copied on write.  Attention through the
+    shared table equals attention over each answer's own contiguous cache."""
+    from exact_attention_tiled_gb300 import workloads
+    n, P, G, bs, H, d = 4, 200, 100, 16, 2, 16
+    q, Kp, Vp, table, seqlens = workloads.shared_prompt_inputs(n, P, G, bs, H, d, seed=70)
+    assert n * math.ceil((P + G) / bs) == 76
+    assert Kp.shape[0] == 40 and len(set(table.flatten().tolist())) == 40
+    assert all((table[i, :P // bs] == table[0, :P // bs]).all() for i in range(n))
+    Kc = torch.stack([Kp[table[i].long()].permute(1, 0, 2, 3).reshape(H, -1, d) for i in range(n)])
+    Vc = torch.stack([Vp[table[i].long()].permute(1, 0, 2, 3).reshape(H, -1, d) for i in range(n)])
+    # every answer sees the same 200 prompt keys, including the copied tail rows
+    for i in range(1, n):
+        assert torch.equal(Kc[i, :, :P], Kc[0, :, :P]) and torch.equal(Vc[i, :, :P], Vc[0, :, :P])
+    Op, Lp = oracle.decode_paged(q, Kp, Vp, table, seqlens)
+    Oc, Lc = oracle.decode(q, Kc, Vc, seqlens)
+    np.testing.assert_array_equal(Op, Oc)
+    np.testing.assert_array_equal(Lp, Lc)

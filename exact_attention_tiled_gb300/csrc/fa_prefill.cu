@@ -109,6 +109,14 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uns
     }
 }
 
+// wait_or_abort for a whole converged warp: every lane polls, and the result
+// is made warp-uniform so the warp never diverges around its elected issues.
+__device__ __forceinline__ bool wait_or_abort_warp(uint32_t bar, uint32_t parity, unsigned *err, int site,
+                                                   volatile int *abort_flag) {
+    const bool ok = wait_or_abort(bar, parity, err, site, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // One work item = one (b, h, pair of 128-row query tiles).
 struct Item {
     int b, h, bh, klen, ntot, t_rel;
@@ -292,8 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (warp == kMmaWarp) {
             // ================================================= MMA issuer
+            // The whole warp runs the loop (warp-uniform control flow and
+            // operands); one elected lane issues each MMA and commit.
             bool issued_any = false;
-            if (lane == 0) {
+            {
                 constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
                 constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);
                 // A descriptor advanced by a byte offset: the start-address
@@ -304,14 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
-                        mma_ss(tmem + t * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+                        mma_ss_warp(tmem + t * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
                     }
                 };
                 auto issue_pv = [&](int t, uint32_t vslot, int j) {
                     const uint64_t vd = sdesc_sw128(vslot, BN * 128, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
-                        mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, vd + ((kk * 2048) >> 4), idesc_o,
+                        mma_ts_warp(tmem + 256 + t * D, tmem + t * 128 + kk * 8, vd + ((kk * 2048) >> 4), idesc_o,
                                (j > 0 || kk > 0) ? 1u : 0u);
                     }
                 };
@@ -325,8 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (k >= num_items) break;
                     const Item it = item_info(p, k, npairs, upb);
                     if (it.ntot == 0) continue;
-                    ok = wait_or_abort(bar_q, qi & 1, p.err, kSiteQ, abort_flag);
-                    if (ok) ok = wait_or_abort(bar_kv_full(g % C::kSlots), (g / C::kSlots) & 1, p.err, kSiteKvFull,
+                    ok = wait_or_abort_warp(bar_q, qi & 1, p.err, kSiteQ, abort_flag);
+                    if (ok) ok = wait_or_abort_warp(bar_kv_full(g % C::kSlots), (g / C::kSlots) & 1, p.err, kSiteKvFull,
                                                abort_flag);
                     if (!ok) break;
                     tc_fence_after();
@@ -335,16 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int t = 0; t < 2; ++t)
                         if (it.nkv[t] > 0) {
                             issue_s(t, ring + (g % C::kSlots) * C::kTileBytes);
-                            mma_commit(bar_s_full(t));
+                            mma_commit_warp(bar_s_full(t));
                         }
                     issued_any = true;
-                    if (it.ntot == 1) mma_commit(bar_q_free);  // the item's last S MMA is issued
+                    if (it.ntot == 1) mma_commit_warp(bar_q_free);  // the item's last S MMA is issued
                     for (int j = 0; ok && j < it.ntot; ++j) {
                         const int iv = g + 2 * j + 1, ik = g + 2 * j + 2;
                         const int sv = iv % C::kSlots, sk = ik % C::kSlots;
                         const uint32_t vslot = ring + sv * C::kTileBytes;
                         const uint32_t kslot = ring + sk * C::kTileBytes;
-                        ok = wait_or_abort(bar_kv_full(sv), (iv / C::kSlots) & 1, p.err, kSiteKvFull, abort_flag);
+                        ok = wait_or_abort_warp(bar_kv_full(sv), (iv / C::kSlots) & 1, p.err, kSiteKvFull, abort_flag);
                         bool k_ready = false;
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
@@ -352,29 +362,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (j < it.nkv[t]) {
                                 // O_t is overwritten by PV_t(0): the previous item's epilogue must have read it
                                 if (j == 0 && uses[t] > 0) {
-                                    ok = wait_or_abort(bar_o_free(t), (uses[t] - 1) & 1, p.err, kSiteO, abort_flag);
+                                    ok = wait_or_abort_warp(bar_o_free(t), (uses[t] - 1) & 1, p.err, kSiteO, abort_flag);
                                     if (!ok) break;
                                 }
-                                ok = wait_or_abort(bar_p_ready(t), pcnt[t] & 1, p.err, kSiteP, abort_flag);
+                                ok = wait_or_abort_warp(bar_p_ready(t), pcnt[t] & 1, p.err, kSiteP, abort_flag);
                                 if (!ok) break;
                                 ++pcnt[t];
                                 tc_fence_after();
                                 issue_pv(t, vslot, j);
-                                if (j + 1 == it.nkv[t]) mma_commit(bar_o_final(t));
+                                if (j + 1 == it.nkv[t]) mma_commit_warp(bar_o_final(t));
                             }
                             if (j + 1 < it.nkv[t]) {
                                 if (!k_ready) {
-                                    ok = wait_or_abort(bar_kv_full(sk), (ik / C::kSlots) & 1, p.err, kSiteKvFull,
+                                    ok = wait_or_abort_warp(bar_kv_full(sk), (ik / C::kSlots) & 1, p.err, kSiteKvFull,
                                                        abort_flag);
                                     if (!ok) break;
                                     tc_fence_after();
                                     k_ready = true;
                                 }
                                 issue_s(t, kslot);
-                                mma_commit(bar_s_full(t));
+                                mma_commit_warp(bar_s_full(t));
                             }
                         }
-                        if (ok && j + 2 == it.ntot) mma_commit(bar_q_free);  // last S MMA of the item issued
+                        if (ok && j + 2 == it.ntot) mma_commit_warp(bar_q_free);  // last S MMA of the item issued
                     }
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
@@ -384,8 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (issued_any) {
                     // every MMA issued above has completed before TMEM is released
-                    mma_commit(bar_mma_done);
+                    mma_commit_warp(bar_mma_done);
                     mbar_wait(bar_mma_done, 0, p.err, kSiteMmaDone);
+                    __syncwarp();
                 }
             }
             __syncwarp();

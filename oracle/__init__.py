@@ -23,5 +23,7 @@ from .oracle import (  # noqa: F401
     sdpa_forward,
     decode,
     decode_paged,
+    sdpa_forward_f64,
+    sdpa_backward,
     max_threads,
 )

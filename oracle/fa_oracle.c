@@ -21,6 +21,11 @@
  *    the (m, l) and (m, l, u) merge with alpha = exp(m_A - m), beta = exp(m_B - m).
  *  - "science-depth M4-055" (airsota.com), "Flash-Decoding Algorithm", step 3:
  *    the log-sum-exp reduction of per-chunk partials (m_k, l_k, O_k).
+ *  - same page, "Backward and recomputation" and "Blocked gradient computation":
+ *    P_ij = exp(S_ij - L_i); dV = P^T dO; dP = dO V^T; dS_ij = P_ij (dP_ij - D_i)
+ *    with D_i = sum_j P_ij dP_ij; dQ = scale dS K; dK = scale dS^T Q.
+ *    CMU 10-423 Lecture 18 notes, section 5.3: the same gradients, with the
+ *    identity D_i = dO_i . O_i (checked by the tests, not used here).
  *  - CMU 10-423 Lecture 18 notes (semidirectx.com), section 2.1: naive, safe
  *    and online softmax; section 2.2 and Exercise 1: the online recurrence
  *    d_j = d_{j-1} exp(m_{j-1} - m_j) + exp(x_j - m_j).
@@ -343,6 +348,157 @@ int oracle_decode_paged(const uint16_t *q, const uint16_t *Kpool, const uint16_t
             bad = 1;
         }
         free(s); free(vr); free(qv);
+    }
+    return bad ? -1 : 0;
+}
+
+/* -------------------------------------------------------------------------
+ * Forward on float64 inputs (the same definition as oracle_sdpa_rows, for
+ * inputs that are not bfloat16 values: the finite-difference checks of the
+ * backward perturb the inputs by amounts bfloat16 cannot represent).
+ * Q, K, V: [B,H,N,d] float64; O_out [B,H,N,d], lse_out [B,H,N].
+ * ------------------------------------------------------------------------- */
+int oracle_sdpa_forward_f64(const double *Q, const double *K, const double *V,
+                            int B, int H, int N, int d, int causal, double scale,
+                            const int32_t *key_len, double *O_out, double *lse_out)
+{
+    if (B < 0 || H < 0 || N < 0 || d <= 0) return -1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    if (!s) return -1;
+    for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
+        const int b = (int)(bh / H);
+        const double *kb = K + (size_t)bh * N * d;
+        const double *vb = V + (size_t)bh * N * d;
+        for (int i = 0; i < N; ++i) {
+            int nvalid = N;
+            if (key_len) nvalid = key_len[b] < nvalid ? key_len[b] : nvalid;
+            if (causal && i + 1 < nvalid) nvalid = i + 1;
+            if (nvalid < 0) nvalid = 0;
+            const double *q = Q + ((size_t)bh * N + i) * d;
+            for (int j = 0; j < nvalid; ++j) {
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c) acc += q[c] * kb[(size_t)j * d + c];
+                s[j] = scale * acc;
+            }
+            oracle_attend_scores(s, vb, nvalid, d, O_out + ((size_t)bh * N + i) * d, lse_out + (size_t)bh * N + i);
+        }
+    }
+    free(s);
+    return 0;
+}
+
+/* -------------------------------------------------------------------------
+ * Backward ("Infra: Flash Attention", "Backward and recomputation" and
+ * "Blocked gradient computation"; CMU 10-423 Lecture 18 notes, 5.3).
+ *
+ * For every (b, h) and query row i, over the valid keys j (key_len, causal
+ * j <= i), with G = dO the upstream gradient:
+ *   S_ij  = scale * Q_i . K_j,   L_i = log sum_j exp(S_ij)
+ *   P_ij  = exp(S_ij - L_i)
+ *   dP_ij = G_i . V_j             (the page's H = G V^T)
+ *   D_i   = sum_j P_ij dP_ij
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dV_j += P_ij G_i,  dK_j += scale dS_ij Q_i,  dQ_i = scale sum_j dS_ij K_j
+ * Rows without a valid key contribute nothing (P = 0).
+ *
+ * Inputs float64 [B,H,N,d]; outputs dQ, dK, dV [B,H,N,d], D and L [B,H,N].
+ * If mag != NULL it receives three arrays [3][B,H,N,d] of term magnitudes
+ * used by the GPU parity tests to bound rounding error per element:
+ *   M_dV[j,c] = sum_i P_ij |G_ic|
+ *   M_dK[j,c] = scale sum_i P_ij (|dP_ij| + A_i) |Q_ic|
+ *   M_dQ[i,c] = scale sum_j P_ij (|dP_ij| + A_i) |K_jc|
+ * with A_i = |D_i| + sum_c |G_ic| |O_ic| (O_i = sum_j P_ij V_j).
+ * Returns 0, or -1 on bad sizes / allocation failure.
+ * ------------------------------------------------------------------------- */
+int oracle_sdpa_backward(const double *Q, const double *K, const double *V, const double *dO,
+                         int B, int H, int N, int d, int causal, double scale, const int32_t *key_len,
+                         double *dQ, double *dK, double *dV, double *D_out, double *L_out,
+                         double *mag, int nthreads)
+{
+    if (B < 0 || H < 0 || N < 0 || d <= 0) return -1;
+    if (nthreads <= 0) nthreads = 1;
+    const size_t total = (size_t)B * H * N * d;
+    memset(dQ, 0, sizeof(double) * total);
+    memset(dK, 0, sizeof(double) * total);
+    memset(dV, 0, sizeof(double) * total);
+    if (mag) memset(mag, 0, sizeof(double) * 3 * total);
+    int bad = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
+        const int b = (int)(bh / H);
+        double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        double *pr = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        double *dp = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!s || !pr || !dp || !o) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            bad = 1;
+            free(s); free(pr); free(dp); free(o);
+            continue;
+        }
+        const size_t base = (size_t)bh * N * d;
+        const double *kb = K + base, *vb = V + base;
+        double *dKb = dK + base, *dVb = dV + base;
+        double *MdV = mag ? mag + base : NULL;
+        double *MdK = mag ? mag + total + base : NULL;
+        double *MdQ = mag ? mag + 2 * total + base : NULL;
+        for (int i = 0; i < N; ++i) {
+            int nvalid = N;
+            if (key_len) nvalid = key_len[b] < nvalid ? key_len[b] : nvalid;
+            if (causal && i + 1 < nvalid) nvalid = i + 1;
+            if (nvalid < 0) nvalid = 0;
+            const double *q = Q + base + (size_t)i * d;
+            const double *g = dO + base + (size_t)i * d;
+            double *dq = dQ + base + (size_t)i * d;
+            if (nvalid == 0) {
+                D_out[(size_t)bh * N + i] = 0.0;
+                L_out[(size_t)bh * N + i] = -INFINITY;
+                continue;
+            }
+            double m = -INFINITY;
+            for (int j = 0; j < nvalid; ++j) {
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c) acc += q[c] * kb[(size_t)j * d + c];
+                s[j] = scale * acc;
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j < nvalid; ++j) l += exp(s[j] - m);
+            const double L = m + log(l);
+            L_out[(size_t)bh * N + i] = L;
+            double D = 0.0;
+            for (int c = 0; c < d; ++c) o[c] = 0.0;
+            for (int j = 0; j < nvalid; ++j) {
+                pr[j] = exp(s[j] - L);
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c) acc += g[c] * vb[(size_t)j * d + c];
+                dp[j] = acc;
+                D += pr[j] * dp[j];
+                for (int c = 0; c < d; ++c) o[c] += pr[j] * vb[(size_t)j * d + c];
+            }
+            D_out[(size_t)bh * N + i] = D;
+            double A = fabs(D);
+            for (int c = 0; c < d; ++c) A += fabs(g[c]) * fabs(o[c]);
+            for (int j = 0; j < nvalid; ++j) {
+                const double ds = pr[j] * (dp[j] - D);
+                const double w = pr[j] * (fabs(dp[j]) + A);
+                for (int c = 0; c < d; ++c) {
+                    dVb[(size_t)j * d + c] += pr[j] * g[c];
+                    dKb[(size_t)j * d + c] += scale * ds * q[c];
+                    dq[c] += scale * ds * kb[(size_t)j * d + c];
+                    if (mag) {
+                        MdV[(size_t)j * d + c] += pr[j] * fabs(g[c]);
+                        MdK[(size_t)j * d + c] += scale * w * fabs(q[c]);
+                        MdQ[(size_t)i * d + c] += scale * w * fabs(kb[(size_t)j * d + c]);
+                    }
+                }
+            }
+        }
+        free(s); free(pr); free(dp); free(o);
     }
     return bad ? -1 : 0;
 }

@@ -83,6 +83,13 @@ def _load():
                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_double, _dp, _dp, ctypes.c_int]
         lib.oracle_decode_paged.restype = ctypes.c_int
+        lib.oracle_sdpa_forward_f64.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_double, _i32p, _dp, _dp]
+        lib.oracle_sdpa_forward_f64.restype = ctypes.c_int
+        lib.oracle_sdpa_backward.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_double, _i32p,
+                                             _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
+        lib.oracle_sdpa_backward.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -324,3 +331,65 @@ def decode_paged(q, Kpool, Vpool, block_table, seqlens, scale=None, nthreads=Non
         raise ValueError("oracle_decode_paged rejected its arguments (table entry out of range?)")
     return O, L
 
+
+
+def _as_f64_4d(x):
+    """float64 copy of a [B, H, N, d] input (torch tensors of any float dtype are widened exactly)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().to(torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    if a.ndim != 4:
+        raise ValueError("expected a [B, H, N, d] array")
+    return a
+
+
+def sdpa_forward_f64(Q, K, V, causal=False, scale=None, key_len=None):
+    """Exact attention on float64 inputs: O [B,H,N,d], L [B,H,N] (single thread)."""
+    q, k, v = _as_f64_4d(Q), _as_f64_4d(K), _as_f64_4d(V)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    kl = _i32(key_len)
+    O = np.empty((B, H, N, d))
+    L = np.empty((B, H, N))
+    rc = _load().oracle_sdpa_forward_f64(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), B, H, N, d,
+                                         int(bool(causal)), float(scale),
+                                         None if kl is None else _ptr(kl, _i32p), _ptr(O, _dp), _ptr(L, _dp))
+    if rc != 0:
+        raise ValueError("oracle_sdpa_forward_f64 rejected its arguments")
+    return O, L
+
+
+def sdpa_backward(Q, K, V, dO, causal=False, scale=None, key_len=None, magnitudes=False, nthreads=None):
+    """Gradients of exact attention with respect to Q, K, V for upstream gradient dO.
+
+    All inputs [B, H, N, d] (bf16 tensors are widened exactly).  Returns a
+    dict with dQ, dK, dV [B,H,N,d], D and L [B,H,N] in float64, and with
+    magnitudes=True also M_dQ, M_dK, M_dV: per-element sums of the terms'
+    magnitudes (see fa_oracle.c) for rounding-error bounds.
+    """
+    q, k, v, g = _as_f64_4d(Q), _as_f64_4d(K), _as_f64_4d(V), _as_f64_4d(dO)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    kl = _i32(key_len)
+    dQ = np.empty((B, H, N, d))
+    dK = np.empty((B, H, N, d))
+    dV = np.empty((B, H, N, d))
+    D = np.empty((B, H, N))
+    L = np.empty((B, H, N))
+    mag = np.empty((3, B, H, N, d)) if magnitudes else None
+    rc = _load().oracle_sdpa_backward(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(g, _dp), B, H, N, d,
+                                      int(bool(causal)), float(scale), None if kl is None else _ptr(kl, _i32p),
+                                      _ptr(dQ, _dp), _ptr(dK, _dp), _ptr(dV, _dp), _ptr(D, _dp), _ptr(L, _dp),
+                                      None if mag is None else _ptr(mag, _dp), _threads(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_sdpa_backward rejected its arguments")
+    out = dict(dQ=dQ, dK=dK, dV=dV, D=D, L=L)
+    if magnitudes:
+        out.update(M_dV=mag[0], M_dK=mag[1], M_dQ=mag[2])
+    return out

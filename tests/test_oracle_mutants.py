@@ -2,8 +2,8 @@
 
 Each case plants one mistake in a temporary copy of the oracle's C source (a
 dropped rescale term, a flipped sign, a wrong operand or index, a missing
-scale or log), builds it, and runs tests/test_oracle_pins.py against that
-copy in a subprocess.  The pin suite must fail for every mutant.  The
+scale or log), builds it, and runs the pin suites (tests/test_oracle_pins.py
+and tests/test_oracle_backward_pins.py) against that copy in a subprocess.  The pin suite must fail for every mutant.  The
 committed oracle itself is never modified.
 """
 import os
@@ -37,6 +37,15 @@ MUTANTS = {
                            "const size_t row = (((size_t)phys * H + h) * bs + (size_t)(t / bs)) * d;"),
     "paged_head_ignored": ("const size_t row = (((size_t)phys * H + h) * bs + (size_t)(t % bs)) * d;",
                            "const size_t row = (((size_t)phys * H + 0) * bs + (size_t)(t % bs)) * d;"),
+    # backward
+    "bwd_drops_D": ("const double ds = pr[j] * (dp[j] - D);", "const double ds = pr[j] * dp[j];"),
+    "bwd_dS_sign": ("const double ds = pr[j] * (dp[j] - D);", "const double ds = pr[j] * (D - dp[j]);"),
+    "bwd_P_unnormalised": ("pr[j] = exp(s[j] - L);", "pr[j] = exp(s[j] - m);"),
+    "bwd_dP_uses_keys": ("acc += g[c] * vb[(size_t)j * d + c];", "acc += g[c] * kb[(size_t)j * d + c];"),
+    "bwd_dV_uses_dS": ("dVb[(size_t)j * d + c] += pr[j] * g[c];", "dVb[(size_t)j * d + c] += ds * g[c];"),
+    "bwd_dK_no_scale": ("dKb[(size_t)j * d + c] += scale * ds * q[c];", "dKb[(size_t)j * d + c] += ds * q[c];"),
+    "bwd_dQ_uses_values": ("dq[c] += scale * ds * kb[(size_t)j * d + c];",
+                           "dq[c] += scale * ds * vb[(size_t)j * d + c];"),
 }
 
 
@@ -44,7 +53,9 @@ MUTANTS = {
 def test_pins_reject_mutant(name, tmp_path):
     old, new = MUTANTS[name]
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    # a mistake is planted everywhere its line appears (the forward's score and
+    # mask lines recur in the float64-input forward and in the backward)
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
     mutant_c = tmp_path / f"{name}.c"
     mutant_c.write_text(src.replace(old, new))
     so = tmp_path / f"{name}.so"
@@ -52,6 +63,7 @@ def test_pins_reject_mutant(name, tmp_path):
                     "-o", str(so), "-lm"], check=True)
     env = dict(os.environ, FA_ORACLE_LIB_OVERRIDE=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_backward_pins.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pin suite passed with mutant {name}:\n{r.stdout[-2000:]}"

@@ -9,6 +9,7 @@ PyTorch fallback, and the calls raise if ``libfa.so`` is missing.
     fa_forward(Q, K, V, causal=False, scale=None, key_len=None) -> (O, L)
     fa_decode(q, Kcache, Vcache, seqlens, num_splits=0, ...)   -> (O, L)
     fa_decode_paged(q, Kpool, Vpool, block_table, seqlens, ...) -> (O, L)
+    fa_backward(Q, K, V, O, dO, L, causal=False, ...)           -> (dQ, dK, dV)
 """
 from __future__ import annotations
 
@@ -16,7 +17,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["fa_forward", "fa_decode", "fa_decode_paged", "fa_decode_plan", "fa_decode_workspace_bytes",
+__all__ = ["fa_forward", "fa_backward", "fa_decode", "fa_decode_paged", "fa_decode_plan", "fa_decode_workspace_bytes",
            "fa_device_error", "FaError", "library", "library_path", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -56,6 +57,11 @@ def library():
         lib.fa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float, _i,
                                   _vp, ctypes.c_size_t, _vp]
         lib.fa_decode.restype = _i
+        lib.fa_backward.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                    ctypes.c_float, _vp, _vp, ctypes.c_size_t, _vp]
+        lib.fa_backward.restype = _i
+        lib.fa_backward_workspace_bytes.argtypes = [_i, _i, _i, _i]
+        lib.fa_backward_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                                          ctypes.c_float, _i, _vp, ctypes.c_size_t, _vp]
         lib.fa_decode_paged.restype = _i
@@ -142,6 +148,43 @@ def fa_forward(Q, K, V, causal=False, scale=None, key_len=None, out=None, lse=No
     if st != 0:
         raise FaError(st, "fa_forward")
     return out, lse
+
+
+def fa_backward(Q, K, V, O, dO, L, causal=False, scale=None, key_len=None, dQ=None, dK=None, dV=None,
+                workspace=None, stream=None):
+    """Gradients (dQ, dK, dV) of exact attention; all bf16 [B, H, N, d] on the GPU.
+
+    O and L are the outputs of fa_forward for the same Q, K, V, causal, scale
+    and key_len; dO is the upstream gradient of O.
+    """
+    torch = _torch()
+    for n, t in (("Q", Q), ("K", K), ("V", V), ("O", O), ("dO", dO)):
+        _check_bf16(n, t, 4)
+        if t.shape != Q.shape:
+            raise ValueError(f"{n} must have the shape of Q")
+    B, H, N, d = Q.shape
+    if L is None or L.dtype != torch.float32 or not L.is_cuda or tuple(L.shape) != (B, H, N):
+        raise TypeError("L must be a CUDA float32 tensor [B, H, N]")
+    L = L.contiguous()
+    if key_len is not None:
+        if key_len.dtype != torch.int32 or not key_len.is_cuda or key_len.numel() != B:
+            raise TypeError("key_len must be a CUDA int32 tensor with B entries")
+        key_len = key_len.contiguous()
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(Q) if dK is None else dK
+    dV = torch.empty_like(Q) if dV is None else dV
+    for n, t in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+        _check_bf16(n, t, 4)
+    need = library().fa_backward_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), device=Q.device, dtype=torch.uint8)
+    st = library().fa_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK),
+                               _ptr(dV), B, H, N, d, int(bool(causal)),
+                               float(scale) if scale is not None else 0.0, _ptr(key_len), _ptr(workspace),
+                               workspace.numel(), _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, "fa_backward")
+    return dQ, dK, dV
 
 
 def fa_decode_plan(B, H, Lmax, d, num_splits=0, seqlens_host=None, num_sms=0):

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_decode.cu", "fa_prefill.cu", "fa_decode_noalloc.cu", "fa_selftest.cu"]
+SOURCES = ["fa_api.cu", "fa_decode.cu", "fa_prefill.cu", "fa_backward.cu", "fa_decode_noalloc.cu",
+           "fa_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -328,6 +328,57 @@ fa_status fa_decode_paged(const void *q, const void *Kpool, const void *Vpool, c
                        num_splits, workspace, workspace_bytes, paged, static_cast<cudaStream_t>(stream));
 }
 
+size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || B > 65535 || H > 65535 || (d != 64 && d != 128)) return 0;
+    return align256(static_cast<size_t>(B) * H * N * sizeof(float));
+}
+
+fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                      const float *L, void *dQ, void *dK, void *dV, int B, int H, int N, int d, int causal,
+                      float scale, const int32_t *key_len, void *workspace, size_t workspace_bytes,
+                      fa_stream_t stream) {
+    if (!Q || !K || !V || !O || !dO || !L || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(dO, 16) ||
+        !aligned(dQ, 16) || !aligned(dK, 16) || !aligned(dV, 16) || !aligned(L, 4) ||
+        (key_len && !aligned(key_len, 4)))
+        return FA_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H * N > (1ll << 40)) return FA_ERR_UNSUPPORTED;
+    if (!(std::isfinite(scale))) return FA_ERR_INVALID_ARG;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(d));
+    const size_t need = fa_backward_workspace_bytes(B, H, N, d);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return FA_ERR_WORKSPACE;
+
+    unsigned *err = nullptr;
+    fa_status s = error_word(&err);
+    if (s != FA_OK) return s;
+
+    BwdParams p;
+    std::memset(&p, 0, sizeof p);
+    p.Q = Q;
+    p.K = K;
+    p.V = V;
+    p.O = O;
+    p.dO = dO;
+    p.L = L;
+    p.Dvec = static_cast<float *>(workspace);
+    p.dQ = dQ;
+    p.dK = dK;
+    p.dV = dV;
+    p.key_len = key_len;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.causal = causal;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+    if (launch_backward(p, d, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
 fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *L, int B, int H,
                      int N, int d, int causal, float scale, const int32_t *key_len,
                      fa_stream_t stream) {

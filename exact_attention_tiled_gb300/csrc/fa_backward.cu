@@ -1,0 +1,651 @@
+// fa_backward.cu -- gradients of exact attention on sm_103a tensor cores.
+//
+// What is computed ("Infra: Flash Attention", "Backward and recomputation"
+// and "Blocked gradient computation"; CMU 10-423 Lecture 18, 5.3): with the
+// forward's per-row log-sum-exp L and the upstream gradient dO,
+//
+//   P_ij  = exp(S_ij - L_i),  S = scale Q K^T      (recomputed tile by tile)
+//   dP_ij = dO_i . V_j
+//   D_i   = dO_i . O_i        (= sum_j P_ij dP_ij, so no pass over P)
+//   dS_ij = P_ij (dP_ij - D_i)
+//   dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K
+//
+// Three kernels, no N x N matrix in global memory:
+//   * bwd_pre_kernel: D = rowsum(dO o O) in fp32 (bandwidth bound).
+//   * bwd_dkdv_kernel: one CTA per 128-key tile j of one (b, h).  K_j and V_j
+//     stay in shared memory; the query tiles i stream through a 2-stage ring
+//     together with their dO_i, L_i and D_i.  Per step the tensor core forms
+//     S^T = K_j Q_i^T and dP^T = V_j dO_i^T in TMEM (keys on the 128 TMEM
+//     lanes, queries on the columns); the compute warpgroup turns them into
+//     P^T and dS^T (bf16, written back over the first half of each), and the
+//     tensor core accumulates dV += P^T dO_i and dK += dS^T Q_i in TMEM with
+//     A read straight from TMEM.  dV, dK leave once, at the end.
+//   * bwd_dq_kernel: one CTA per 128-query tile i: S = Q_i K_j^T and
+//     dP = dO_i V_j^T per key tile, dS in the compute warpgroup, and
+//     dQ += dS K_j in TMEM.  Computing dQ in its own pass (recomputing S and
+//     dP) keeps every gradient element written by exactly one CTA: no atomics,
+//     and the result does not depend on scheduling.
+// Warp roles in both main kernels (256 threads): warp 0 lane 0 issues the
+// TMA copies, warp 1 is the MMA warp (converged, one elected lane issues),
+// warps 4-7 are the compute warpgroup, one thread per TMEM lane (tile row).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+#include "fa_tmap.h"
+
+namespace fa {
+namespace {
+
+constexpr int BT = 128;              // rows of a query or key tile (MMA M and N)
+constexpr int kBwdThreads = 256;
+constexpr int kProd = 0, kMma = 1, kFirstCompute = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum {
+    kSiteBwKV = 0x401, kSiteBwQD = 0x402, kSiteBwS = 0x403, kSiteBwP = 0x404, kSiteBwDone = 0x405,
+    kSiteBwEmpty = 0x406, kSiteBwDrain = 0x407
+};
+
+struct BwdMaps {
+    CUtensorMap q, k, v, dO;
+};
+
+__device__ __forceinline__ bool wait_abort(uint32_t bar, uint32_t parity, unsigned *err, int site,
+                                           volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            report_timeout(err, site);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// converged-warp form: every lane polls, the result is warp-uniform
+__device__ __forceinline__ bool wait_abort_warp(uint32_t bar, uint32_t parity, unsigned *err, int site,
+                                                volatile int *abort_flag) {
+    return __all_sync(0xffffffffu, wait_abort(bar, parity, err, site, abort_flag));
+}
+
+__device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kColBlocks = D / 64;
+    static constexpr int kTileBytes = BT * D * 2;
+    static constexpr int kStages = 2;
+    // dkdv: K, V, then per stage {Q_i, dO_i}, then per stage {L_i * log2 e, D_i}
+    // dq:   Q, dO, then per stage {K_j, V_j}
+    static constexpr int kFixedOff = 0;
+    static constexpr int kStageOff = 2 * kTileBytes;
+    static constexpr int kVecOff = kStageOff + kStages * 2 * kTileBytes;
+    static constexpr int kBarOff = kVecOff + kStages * 2 * BT * 4;
+    static constexpr int kNumBars = 16;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    // at least 120 KB, so one CTA per SM: each allocates all 512 TMEM columns
+    static constexpr int kSmemUsed = kMiscOff + 16 + 1024;
+    static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
+};
+
+// TMEM: [0,128) S (then P), [128,256) dP (then dS), [256, 256+D) dV or dQ,
+// [256+D, 256+2D) dK.  P and dS are written as packed bf16 pairs over the
+// first 64 columns of their region: the A operand of the second GEMMs.
+constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
+
+// ---------------------------------------------------------------------------
+// D_i = sum_c dO_ic O_ic.  D/8 lanes per row, one 16-byte vector each.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *O, const __nv_bfloat16 *dO,
+                                                      float *Dout, long long rows) {
+    constexpr int LPR = D / 8;
+    const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long row = gtid / LPR;
+    const int part = static_cast<int>(gtid % LPR);
+    float acc = 0.f;
+    if (row < rows) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(O + row * D + part * 8);
+        const uint4 b = *reinterpret_cast<const uint4 *>(dO + row * D + part * 8);
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc = fmaf(__uint_as_float(wa[i] << 16), __uint_as_float(wb[i] << 16), acc);
+            acc = fmaf(__uint_as_float(wa[i] & 0xFFFF0000u), __uint_as_float(wb[i] & 0xFFFF0000u), acc);
+        }
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && part == 0) Dout[row] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// dK, dV: grid (B*H, ceil(N/128)); blockIdx.y = key tile (heaviest first
+// under causal masking: key tile j meets the query tiles i >= j).
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t k_smem = sbase + C::kFixedOff, v_smem = k_smem + C::kTileBytes;
+    auto q_stage = [&](int s) { return sbase + C::kStageOff + s * 2 * C::kTileBytes; };
+    auto do_stage = [&](int s) { return q_stage(s) + C::kTileBytes; };
+    float *vec = reinterpret_cast<float *>(smem + C::kVecOff);   // [stage][2][BT]: L*log2e, D
+    const uint32_t bars = sbase + C::kBarOff;
+    const uint32_t bar_kv = bars;
+    auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto bar_empty = [&](int s) { return bars + 8u * (3 + s); };
+    const uint32_t bar_st = bars + 8u * 5, bar_ps = bars + 8u * 6, bar_done = bars + 8u * 7;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x, jt = blockIdx.y;
+    const int b = bh / p.H;
+    const int N = p.N;
+    const int T = (N + BT - 1) / BT;
+    int klen = N;
+    if (p.key_len) klen = clampi(p.key_len[b], 0, N);
+    const int key0 = jt * BT;
+    // query tiles this key tile meets; none when every key of the tile is masked
+    const int i_lo = p.causal ? jt : 0;
+    const int nsteps = key0 < klen ? T - i_lo : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_kv, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar_full(s), 2);    // TMA bytes + the producer warp's L/D stores
+            mbar_init(bar_empty(s), 1);
+        }
+        mbar_init(bar_st, 1);
+        mbar_init(bar_ps, 4);
+        mbar_init(bar_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMma) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProd) {
+        // ================================================= producer warp
+        bool ok = true;
+        if (nsteps > 0) {
+            if (lane == 0) {
+                prefetch_tmap(&tm.q);
+                prefetch_tmap(&tm.k);
+                prefetch_tmap(&tm.v);
+                prefetch_tmap(&tm.dO);
+                const uint64_t pol = l2_policy_evict_normal();
+                mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
+#pragma unroll
+                for (int cb = 0; cb < C::kColBlocks; ++cb) {
+                    tma_load_3d(k_smem + cb * (BT * 128), &tm.k, cb * 64, key0, bh, bar_kv, pol);
+                    tma_load_3d(v_smem + cb * (BT * 128), &tm.v, cb * 64, key0, bh, bar_kv, pol);
+                }
+            }
+            for (int n = 0; n < nsteps && ok; ++n) {
+                const int s = n % C::kStages;
+                const int i = i_lo + n;
+                if (n >= C::kStages)
+                    ok = __all_sync(0xffffffffu, wait_abort(bar_empty(s), ((n / C::kStages) - 1) & 1, p.err,
+                                                             kSiteBwEmpty, abort_flag));
+                if (!ok) break;
+                if (lane == 0) {
+                    const uint64_t pol = l2_policy_evict_normal();
+                    mbar_arrive_expect_tx(bar_full(s), 2 * C::kTileBytes);
+#pragma unroll
+                    for (int cb = 0; cb < C::kColBlocks; ++cb) {
+                        tma_load_3d(q_stage(s) + cb * (BT * 128), &tm.q, cb * 64, i * BT, bh, bar_full(s), pol);
+                        tma_load_3d(do_stage(s) + cb * (BT * 128), &tm.dO, cb * 64, i * BT, bh, bar_full(s), pol);
+                    }
+                }
+                // L_i * log2(e) and D_i of this query tile (rows past N: never used)
+                float *lv = vec + s * 2 * BT;
+#pragma unroll
+                for (int e = 0; e < BT / 32; ++e) {
+                    const int q = i * BT + e * 32 + lane;
+                    const size_t idx = static_cast<size_t>(bh) * N + q;
+                    lv[e * 32 + lane] = q < N ? p.L[idx] * kLog2e : 0.f;
+                    lv[BT + e * 32 + lane] = q < N ? p.Dvec[idx] : 0.f;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_full(s));
+            }
+            // no copy may be in flight when the CTA exits
+            if (lane == 0) {
+                mbar_wait(bar_kv, 0, p.err, kSiteBwDrain);
+                const int first = nsteps > C::kStages ? nsteps - C::kStages : 0;
+                for (int n = first; n < nsteps; ++n)
+                    mbar_wait(bar_full(n % C::kStages), (n / C::kStages) & 1, p.err, kSiteBwDrain);
+            }
+        }
+    } else if (warp == kMma) {
+        // ================================================= MMA warp
+        if (nsteps > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, 0, 0);
+            constexpr uint32_t idesc_g = idesc_bf16_f32(BT, D, 0, 1);
+            bool ok = wait_abort_warp(bar_kv, 0, p.err, kSiteBwKV, abort_flag);
+            for (int n = 0; n < nsteps && ok; ++n) {
+                const int s = n % C::kStages;
+                ok = wait_abort_warp(bar_full(s), (n / C::kStages) & 1, p.err, kSiteBwQD, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                {   // S^T = K Q_i^T and dP^T = V dO_i^T (K-major A and B)
+                    const uint64_t kd = sdesc_sw128(k_smem, 16, 1024), vd = sdesc_sw128(v_smem, 16, 1024);
+                    const uint64_t qd = sdesc_sw128(q_stage(s), 16, 1024), od = sdesc_sw128(do_stage(s), 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+                        mma_ss_warp(tmem + kColS, kd + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+                        mma_ss_warp(tmem + kColDP, vd + off, od + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit_warp(bar_st);
+                ok = wait_abort_warp(bar_ps, n & 1, p.err, kSiteBwP, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                {   // dV += P^T dO_i, dK += dS^T Q_i (A from TMEM, B MN-major: d contiguous)
+                    const uint64_t odm = sdesc_sw128(do_stage(s), BT * 128, 1024);
+                    const uint64_t qdm = sdesc_sw128(q_stage(s), BT * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ts_warp(tmem + kColAcc, tmem + kColS + kk * 8, odm + ((kk * 2048) >> 4), idesc_g,
+                                    (n > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ts_warp(tmem + kColAcc + D, tmem + kColDP + kk * 8, qdm + ((kk * 2048) >> 4), idesc_g,
+                                    (n > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit_warp(bar_empty(s));   // Q_i, dO_i read: the stage is free
+            }
+            // every MMA has completed before the gradients are read and TMEM is freed
+            mma_commit_warp(bar_done);
+            mbar_wait(bar_done, 0, p.err, kSiteBwDone);
+            __syncwarp();
+        }
+    } else if (warp >= kFirstCompute) {
+        // ================================================= compute warpgroup
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;      // key row of the tile
+        const int key = key0 + r;
+        const bool key_ok = key < klen;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const float sl2 = p.scale_log2;
+        bool ok = true;
+        for (int n = 0; n < nsteps && ok; ++n) {
+            const int s = n % C::kStages;
+            const int q0 = (i_lo + n) * BT;
+            ok = wait_abort_warp(bar_st, n & 1, p.err, kSiteBwS, abort_flag);
+            // the producer warp's L_i / D_i stores are published by the stage's
+            // full barrier (already complete here: the MMAs behind bar_st waited on it)
+            if (ok) ok = wait_abort_warp(bar_full(s), (n / C::kStages) & 1, p.err, kSiteBwQD, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            __syncwarp();
+            const float *lv = vec + s * 2 * BT;     // L_i * log2 e
+            const float *dv = lv + BT;              // D_i
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_off + kColS + c * 32, sr);
+                tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
+                tmem_wait_ld();
+                reg_fence(sr);
+                reg_fence(dr);
+                uint32_t pp[16], dp[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float pv[2], dsv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int col = c * 32 + e + u;
+                        const int q = q0 + col;
+                        const bool valid = key_ok && q < N && (!p.causal || key <= q);
+                        const float x = fmaf(__uint_as_float(sr[e + u]), sl2, -lv[col]);
+                        const float pr = valid ? ex2(x) : 0.f;
+                        pv[u] = pr;
+                        dsv[u] = pr * (__uint_as_float(dr[e + u]) - dv[col]);
+                    }
+                    pp[e >> 1] = pack_bf16(pv[0], pv[1]);
+                    dp[e >> 1] = pack_bf16(dsv[0], dsv[1]);
+                }
+                // packed columns 16c..16c+15 lie in chunks already read
+                tmem_st16(tmem + lane_off + kColS + c * 16, pp);
+                tmem_st16(tmem + lane_off + kColDP + c * 16, dp);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_ps);
+        }
+        // ---- epilogue: dV and dK (x scale) to bf16; keys with no step get zeros
+        if (ok && nsteps > 0) {
+            ok = wait_abort_warp(bar_done, 0, p.err, kSiteBwDone, abort_flag);
+            tc_fence_after();
+            __syncwarp();
+        }
+        // tcgen05.ld is warp-collective: every lane loads, only rows < N store
+        if (ok) {
+            const size_t row = (static_cast<size_t>(bh) * N + (key < N ? key : 0)) * D;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(which ? p.dK : p.dV) + row;
+                const float mul = which ? p.scale : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t a[32];
+                    if (nsteps > 0) {
+                        tmem_ld32(tmem + lane_off + kColAcc + which * D + c * 32, a);
+                        tmem_wait_ld();
+                        reg_fence(a);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) a[e] = 0u;
+                    }
+                    if (key < N) {
+                        uint4 *out = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            out[v] = make_uint4(
+                                pack_bf16(__uint_as_float(a[8 * v]) * mul, __uint_as_float(a[8 * v + 1]) * mul),
+                                pack_bf16(__uint_as_float(a[8 * v + 2]) * mul, __uint_as_float(a[8 * v + 3]) * mul),
+                                pack_bf16(__uint_as_float(a[8 * v + 4]) * mul, __uint_as_float(a[8 * v + 5]) * mul),
+                                pack_bf16(__uint_as_float(a[8 * v + 6]) * mul, __uint_as_float(a[8 * v + 7]) * mul));
+                    }
+                    __syncwarp();   // reconverge before the next warp-collective load
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMma) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// dQ: grid (B*H, ceil(N/128)); blockIdx.y = query tile rank, heaviest first
+// under causal masking (query tile i meets the key tiles j <= i).
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t q_smem = sbase + C::kFixedOff, do_smem = q_smem + C::kTileBytes;
+    auto k_stage = [&](int s) { return sbase + C::kStageOff + s * 2 * C::kTileBytes; };
+    auto v_stage = [&](int s) { return k_stage(s) + C::kTileBytes; };
+    const uint32_t bars = sbase + C::kBarOff;
+    const uint32_t bar_qd = bars;
+    auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto bar_empty = [&](int s) { return bars + 8u * (3 + s); };
+    const uint32_t bar_st = bars + 8u * 5, bar_ps = bars + 8u * 6, bar_done = bars + 8u * 7;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int b = bh / p.H;
+    const int N = p.N;
+    const int T = (N + BT - 1) / BT;
+    const int it = T - 1 - static_cast<int>(blockIdx.y);
+    const int q0 = it * BT;
+    int klen = N;
+    if (p.key_len) klen = clampi(p.key_len[b], 0, N);
+    int kend = klen;
+    if (p.causal) kend = min(kend, min(N, q0 + BT));
+    const int nsteps = (kend + BT - 1) / BT;    // key tiles 0 .. nsteps-1
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_qd, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar_full(s), 1);
+            mbar_init(bar_empty(s), 1);
+        }
+        mbar_init(bar_st, 1);
+        mbar_init(bar_ps, 4);
+        mbar_init(bar_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMma) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProd) {
+        if (lane == 0 && nsteps > 0) {
+            prefetch_tmap(&tm.q);
+            prefetch_tmap(&tm.k);
+            prefetch_tmap(&tm.v);
+            prefetch_tmap(&tm.dO);
+            const uint64_t pol = l2_policy_evict_normal();
+            mbar_arrive_expect_tx(bar_qd, 2 * C::kTileBytes);
+#pragma unroll
+            for (int cb = 0; cb < C::kColBlocks; ++cb) {
+                tma_load_3d(q_smem + cb * (BT * 128), &tm.q, cb * 64, q0, bh, bar_qd, pol);
+                tma_load_3d(do_smem + cb * (BT * 128), &tm.dO, cb * 64, q0, bh, bar_qd, pol);
+            }
+            bool ok = true;
+            for (int n = 0; n < nsteps && ok; ++n) {
+                const int s = n % C::kStages;
+                if (n >= C::kStages) {
+                    ok = wait_abort(bar_empty(s), ((n / C::kStages) - 1) & 1, p.err, kSiteBwEmpty, abort_flag);
+                    if (!ok) break;
+                }
+                mbar_arrive_expect_tx(bar_full(s), 2 * C::kTileBytes);
+#pragma unroll
+                for (int cb = 0; cb < C::kColBlocks; ++cb) {
+                    tma_load_3d(k_stage(s) + cb * (BT * 128), &tm.k, cb * 64, n * BT, bh, bar_full(s), pol);
+                    tma_load_3d(v_stage(s) + cb * (BT * 128), &tm.v, cb * 64, n * BT, bh, bar_full(s), pol);
+                }
+            }
+            mbar_wait(bar_qd, 0, p.err, kSiteBwDrain);
+            const int first = nsteps > C::kStages ? nsteps - C::kStages : 0;
+            for (int n = first; n < nsteps; ++n)
+                mbar_wait(bar_full(n % C::kStages), (n / C::kStages) & 1, p.err, kSiteBwDrain);
+        }
+    } else if (warp == kMma) {
+        if (nsteps > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, 0, 0);
+            constexpr uint32_t idesc_g = idesc_bf16_f32(BT, D, 0, 1);
+            bool ok = wait_abort_warp(bar_qd, 0, p.err, kSiteBwQD, abort_flag);
+            const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), od = sdesc_sw128(do_smem, 16, 1024);
+            for (int n = 0; n < nsteps && ok; ++n) {
+                const int s = n % C::kStages;
+                ok = wait_abort_warp(bar_full(s), (n / C::kStages) & 1, p.err, kSiteBwKV, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                {   // S = Q K_j^T, dP = dO V_j^T
+                    const uint64_t kd = sdesc_sw128(k_stage(s), 16, 1024), vd = sdesc_sw128(v_stage(s), 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+                        mma_ss_warp(tmem + kColS, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+                        mma_ss_warp(tmem + kColDP, od + off, vd + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit_warp(bar_st);
+                ok = wait_abort_warp(bar_ps, n & 1, p.err, kSiteBwP, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                {   // dQ += dS K_j (A = dS from TMEM, B = K_j MN-major)
+                    const uint64_t kdm = sdesc_sw128(k_stage(s), BT * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ts_warp(tmem + kColAcc, tmem + kColDP + kk * 8, kdm + ((kk * 2048) >> 4), idesc_g,
+                                    (n > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit_warp(bar_empty(s));
+            }
+            mma_commit_warp(bar_done);
+            mbar_wait(bar_done, 0, p.err, kSiteBwDone);
+            __syncwarp();
+        }
+    } else if (warp >= kFirstCompute) {
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int q = q0 + r;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const float sl2 = p.scale_log2;
+        float lrow = 0.f, drow = 0.f;
+        if (q < N) {
+            lrow = p.L[static_cast<size_t>(bh) * N + q] * kLog2e;
+            drow = p.Dvec[static_cast<size_t>(bh) * N + q];
+        }
+        bool ok = true;
+        for (int n = 0; n < nsteps && ok; ++n) {
+            ok = wait_abort_warp(bar_st, n & 1, p.err, kSiteBwS, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            __syncwarp();
+            const int kb = n * BT;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_off + kColS + c * 32, sr);
+                tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
+                tmem_wait_ld();
+                reg_fence(sr);
+                reg_fence(dr);
+                uint32_t dp[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float dsv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int key = kb + c * 32 + e + u;
+                        const bool valid = q < N && key < klen && (!p.causal || key <= q);
+                        const float pr = valid ? ex2(fmaf(__uint_as_float(sr[e + u]), sl2, -lrow)) : 0.f;
+                        dsv[u] = pr * (__uint_as_float(dr[e + u]) - drow);
+                    }
+                    dp[e >> 1] = pack_bf16(dsv[0], dsv[1]);
+                }
+                tmem_st16(tmem + lane_off + kColDP + c * 16, dp);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_ps);
+        }
+        if (ok && nsteps > 0) {
+            ok = wait_abort_warp(bar_done, 0, p.err, kSiteBwDone, abort_flag);
+            tc_fence_after();
+            __syncwarp();
+        }
+        // tcgen05.ld is warp-collective: every lane loads, only rows < N store
+        if (ok) {
+            __nv_bfloat16 *dst =
+                static_cast<__nv_bfloat16 *>(p.dQ) + (static_cast<size_t>(bh) * N + (q < N ? q : 0)) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t a[32];
+                if (nsteps > 0) {
+                    tmem_ld32(tmem + lane_off + kColAcc + c * 32, a);
+                    tmem_wait_ld();
+                    reg_fence(a);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) a[e] = 0u;
+                }
+                if (q < N) {
+                    const float mul = p.scale;
+                    uint4 *out = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        out[v] = make_uint4(
+                            pack_bf16(__uint_as_float(a[8 * v]) * mul, __uint_as_float(a[8 * v + 1]) * mul),
+                            pack_bf16(__uint_as_float(a[8 * v + 2]) * mul, __uint_as_float(a[8 * v + 3]) * mul),
+                            pack_bf16(__uint_as_float(a[8 * v + 4]) * mul, __uint_as_float(a[8 * v + 5]) * mul),
+                            pack_bf16(__uint_as_float(a[8 * v + 6]) * mul, __uint_as_float(a[8 * v + 7]) * mul));
+                }
+                __syncwarp();   // reconverge before the next warp-collective load
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMma) tmem_dealloc(tmem, 512);
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(p.B) * p.H * p.N;
+    {
+        constexpr int LPR = D / 8;
+        const long long threads = rows * LPR;
+        const long long blocks = (threads + 255) / 256;
+        if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+        bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(p.O), static_cast<const __nv_bfloat16 *>(p.dO), p.Dvec, rows);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    BwdMaps tm;
+    std::memset(&tm, 0, sizeof tm);
+    const int BH = p.B * p.H;
+    if (!make_map(&tm.q, p.Q, BH, p.N, D) || !make_map(&tm.k, p.K, BH, p.N, D) ||
+        !make_map(&tm.v, p.V, BH, p.N, D) || !make_map(&tm.dO, p.dO, BH, p.N, D))
+        return cudaErrorInvalidValue;
+    const int smem = BwdCfg<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int T = (p.N + BT - 1) / BT;
+    const dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(T));
+    bwd_dkdv_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tm, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_dq_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tm, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BwdParams &p, int d, cudaStream_t stream) {
+    return d == 128 ? launch_bwd_d<128>(p, stream) : launch_bwd_d<64>(p, stream);
+}
+
+}  // namespace fa

@@ -52,6 +52,22 @@ struct PrefillParams {
 
 cudaError_t launch_prefill(const PrefillParams &p, int d, cudaStream_t stream);
 
+// ------------------------------------------------------------------ backward
+struct BwdParams {
+    const void *Q, *K, *V, *O, *dO;   // bf16 [B, H, N, d]
+    const float *L;                   // fp32 [B, H, N], the forward's natural-log LSE
+    float *Dvec;                      // fp32 [B, H, N] scratch: D_i = dO_i . O_i
+    void *dQ, *dK, *dV;               // bf16 [B, H, N, d]
+    const int32_t *key_len;           // device [B] or nullptr
+    int B, H, N;
+    int causal;
+    float scale;                      // score multiplier
+    float scale_log2;                 // scale * log2(e)
+    unsigned *err;
+};
+
+cudaError_t launch_backward(const BwdParams &p, int d, cudaStream_t stream);
+
 // ------------------------------------------------------------------ self-test
 constexpr int kSiteSelfTest = 0x301;
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned *err, cudaStream_t stream);

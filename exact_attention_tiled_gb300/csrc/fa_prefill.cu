@@ -53,6 +53,7 @@
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_tmap.h"
 
 namespace fa {
 namespace {
@@ -435,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float r_base = -INFINITY;
             float l_run = 0.f;
             for (int j = 0; j < my_nkv; ++j) {
-                ok = wait_or_abort(bar_s_full(t), scnt & 1, p.err, kSiteS, abort_flag);
+                ok = __all_sync(0xffffffffu, wait_or_abort(bar_s_full(t), scnt & 1, p.err, kSiteS, abort_flag));
                 if (!ok) break;
                 ++scnt;
                 // S_t(j) complete implies every MMA issued before it is complete:
@@ -553,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ---- epilogue: O = U / l, L = m + log l
             if (my_nkv > 0) {
-                ok = wait_or_abort(bar_o_final(t), uses & 1, p.err, kSiteO, abort_flag);
+                ok = __all_sync(0xffffffffu, wait_or_abort(bar_o_final(t), uses & 1, p.err, kSiteO, abort_flag));
                 if (!ok) break;
                 ++uses;
                 tc_fence_after();
@@ -610,40 +611,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-// 3-D view [B*H][N][d] of a bf16 tensor; box = 64 columns x 128 rows x 1.
-bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                          static_cast<cuuint64_t>(BH)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-    cuuint32_t box[3] = {64, 128, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
     TmapSet tm;

@@ -1,7 +1,7 @@
 /*
  * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library (libfa.so).
  *
- * Two operations, both defined by the pages this library follows:
+ * The operations, all defined by the pages this library follows:
  *
  *   fa_forward  exact scaled-dot-product attention O = softmax(Q K^T * scale) V,
  *               computed tile by tile with the online-softmax state (m, l, U)
@@ -91,6 +91,40 @@ typedef void *fa_stream_t; /* cudaStream_t */
 FA_API fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *L,
                      int B, int H, int N, int d, int causal, float scale,
                      const int32_t *key_len, fa_stream_t stream);
+
+/*
+ * fa_backward -- gradients of exact attention ("Infra: Flash Attention",
+ * sections "Backward and recomputation" and "Blocked gradient computation";
+ * CMU 10-423 Lecture 18 notes, 5.3).  With S = scale Q K^T (masked as in
+ * fa_forward), P_ij = exp(S_ij - L_i), dP = dO V^T, D_i = dO_i . O_i and
+ * dS_ij = P_ij (dP_ij - D_i):
+ *     dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K.
+ * P, dP and dS are recomputed tile by tile on chip and never reach global
+ * memory.
+ *
+ *   Q, K, V, O, dO  bf16 [B, H, N, d]: the forward's inputs and output and the
+ *                   upstream gradient of O.
+ *   L               float [B, H, N]: the forward's L for the same inputs.
+ *   dQ, dK, dV      bf16 [B, H, N, d] outputs, fully written (keys that no
+ *                   query sees, and query rows with no valid key, get 0).
+ *   B, H, N, d, causal, scale, key_len: as in fa_forward (same values as the
+ *                   forward call that produced O and L).
+ *   workspace       device scratch of at least fa_backward_workspace_bytes()
+ *                   bytes, 256-byte aligned (holds D); not read before written.
+ *
+ * Arithmetic: fp32 tensor-core accumulation; P and dS are rounded to bf16
+ * before the products with dO, Q and K; D from the bf16 O.  Every gradient
+ * element is written by one thread block (no atomics): results do not
+ * depend on scheduling.
+ */
+FA_API fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O,
+                             const void *dO, const float *L, void *dQ, void *dK, void *dV,
+                             int B, int H, int N, int d, int causal, float scale,
+                             const int32_t *key_len, void *workspace, size_t workspace_bytes,
+                             fa_stream_t stream);
+
+/* Workspace bytes fa_backward needs (0 for arguments it would reject). */
+FA_API size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
 
 /*
  * fa_decode -- split-KV single-query attention (Flash-Decoding).

@@ -194,3 +194,27 @@ def test_paged_inputs_structure():
     assert len(set(used)) == len(used) and all(0 <= u < Kp.shape[0] for u in used)
     assert used != sorted(used)                # blocks are scattered, not in logical order
     assert sl.tolist() == lens
+
+
+def _bwd(lib, **kw):
+    a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, dO=FAKE, L=FAKE, dQ=FAKE, dK=FAKE, dV=FAKE, B=1, H=2, N=256, d=64,
+             causal=0, scale=0.0, kl=None, ws=FAKE, wsb=1 << 20)
+    a.update(kw)
+    return lib.fa_backward(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["L"], a["dQ"], a["dK"], a["dV"], a["B"],
+                           a["H"], a["N"], a["d"], a["causal"], ctypes.c_float(a["scale"]), a["kl"], a["ws"],
+                           a["wsb"], None)
+
+
+def test_backward_rejects_bad_arguments_before_cuda(lib):
+    assert _bwd(lib, dO=None) == 1
+    assert _bwd(lib, L=None) == 1
+    assert _bwd(lib, dK=FAKE + 8) == 1
+    assert _bwd(lib, L=FAKE + 2) == 1
+    assert _bwd(lib, N=0) == 1
+    assert _bwd(lib, causal=3) == 1
+    assert _bwd(lib, scale=float("inf")) == 1
+    assert _bwd(lib, d=32) == 2
+    assert _bwd(lib, ws=None) == 4
+    assert _bwd(lib, wsb=16) == 4
+    assert lib.fa_backward_workspace_bytes(2, 3, 1000, 128) == (2 * 3 * 1000 * 4 + 255) // 256 * 256
+    assert lib.fa_backward_workspace_bytes(2, 3, 1000, 96) == 0

@@ -62,8 +62,9 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
-    "prefill_kernel": ("fa_prefill.cu", "fa_ptx.cuh", "fa_internal.h"),
+    "prefill_kernel": ("fa_prefill.cu", "fa_ptx.cuh", "fa_internal.h", "fa_tmap.h"),
     "decode_split_kernel": ("fa_decode.cu", "fa_ptx.cuh", "fa_internal.h"),
+    "bwd_dkdv_kernel": ("fa_backward.cu", "fa_ptx.cuh", "fa_internal.h", "fa_tmap.h"),
 }
 
 
@@ -312,6 +313,25 @@ def run_ours(args, rank, world, local_rank):
             "frac_of_hbm_peak": round(byp / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "block_size": bs, "num_blocks": int(Kp.shape[0])}
         del qp, Kp, Vp
+    # backward (dQ, dK, dV) of the two prefill shapes; algorithmic FLOPs = 5 GEMMs of 2 d per
+    # unmasked score = 2.5 x the forward's (CMU 10-423 Lecture 18, 6.1: 10 N^2 d per head)
+    for name, (B_, H_, N_, d_, causal_, amp_, seed_) in (
+            ("backward_causal_b1h32_n8192_d128", (wp.B, wp.H, wp.N, wp.d, True, 1.0, wp.seed)),
+            ("backward_b8h16_n2048_d64", (w3.B, w3.H, w3.N, w3.d, False, w3.amp, w3.seed))):
+        Qb, Kb, Vb = workloads.prefill_inputs(B_, H_, N_, d_, seed_, amp_, device=dev)
+        gb = torch.Generator(device=dev)
+        gb.manual_seed(seed_ + 1000)
+        dOb = torch.randn(Qb.shape, generator=gb, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        Ob, Lb = fa.fa_forward(Qb, Kb, Vb, causal=causal_)
+        dQb, dKb, dVb = torch.empty_like(Qb), torch.empty_like(Qb), torch.empty_like(Qb)
+        wsb = torch.empty(fa.fa_backward_workspace_bytes(B_, H_, N_, d_), device=dev, dtype=torch.uint8)
+        ms = timed(lambda: fa.fa_backward(Qb, Kb, Vb, Ob, dOb, Lb, causal=causal_, dQ=dQb, dK=dKb, dV=dVb,
+                                          workspace=wsb))
+        fl = 2.5 * prefill_flops(B_, H_, N_, d_, causal_)
+        others[name] = {"ms": round(ms, 4), "flops": fl, "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+                        "frac_of_bf16_peak": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                        "kernels": "bwd_pre + bwd_dkdv + bwd_dq (S and dP recomputed in both)"}
+        del Qb, Kb, Vb, dOb, Ob, Lb, dQb, dKb, dVb
     st, site = fa.fa_device_error(clear=True)
     if st != 0:
         raise RuntimeError(f"device error word set by the other workloads (site {site:#x})")
@@ -490,6 +510,15 @@ def run_profile_case(args):
         wp = workloads.WORKLOADS[PREFILL]
         Q, K, V = workloads.prefill_inputs(wp.B, wp.H, wp.N, wp.d, wp.seed, device=dev)
         run = lambda: fa.fa_forward(Q, K, V, causal=True)
+    elif args.profile == "backward":
+        # the batched d64 shape (B8 H16 N2048): ~0.3 GB on the device
+        w3 = workloads.WORKLOADS["prefill_b8h16_n2048_d64"]
+        Q, K, V = workloads.prefill_inputs(w3.B, w3.H, w3.N, w3.d, w3.seed, w3.amp, device=dev)
+        gb = torch.Generator(device=dev)
+        gb.manual_seed(w3.seed + 1000)
+        dO = torch.randn(Q.shape, generator=gb, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        O, L = fa.fa_forward(Q, K, V)
+        run = lambda: fa.fa_backward(Q, K, V, O, dO, L)
     else:
         wd = workloads.WORKLOADS[DECODE]
         q, Kc, Vc = workloads.decode_inputs(wd.B, wd.H, wd.N, wd.d, wd.seed, device=dev)
@@ -513,7 +542,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "backward"], default=None,
                     help="only launch one kernel warmup+steps times (for ncu captures)")
     ap.add_argument("--record-traffic", nargs=3, metavar=("REPORT", "KERNEL", "NOTE"), default=None,
                     help="write DRAM bytes per launch of KERNEL from an ncu report to profiles/")

@@ -17,7 +17,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["fa_forward", "fa_backward", "fa_decode", "fa_decode_paged", "fa_decode_plan", "fa_decode_workspace_bytes",
+__all__ = ["fa_forward", "fa_backward", "fa_backward_workspace_bytes", "fa_decode", "fa_decode_paged", "fa_decode_plan", "fa_decode_workspace_bytes",
            "fa_device_error", "FaError", "library", "library_path", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -148,6 +148,10 @@ def fa_forward(Q, K, V, causal=False, scale=None, key_len=None, out=None, lse=No
     if st != 0:
         raise FaError(st, "fa_forward")
     return out, lse
+
+
+def fa_backward_workspace_bytes(B, H, N, d):
+    return int(library().fa_backward_workspace_bytes(B, H, N, d))
 
 
 def fa_backward(Q, K, V, O, dO, L, causal=False, scale=None, key_len=None, dQ=None, dK=None, dV=None,

@@ -311,6 +311,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __syncwarp();
             const float *lv = vec + s * 2 * BT;     // L_i * log2 e
             const float *dv = lv + BT;              // D_i
+            // masking only where the tile touches key_len, the sequence end or the diagonal
+            const bool need_mask = key0 + BT > klen || q0 + BT > N || (p.causal && key0 + BT - 1 > q0);
+            const float2 sl22 = make_float2(sl2, sl2);
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t sr[32], dr[32];
@@ -319,22 +322,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_wait_ld();
                 reg_fence(sr);
                 reg_fence(dr);
-                uint32_t pp[16], dp[16];
+                if (need_mask) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float pv[2], dsv[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int col = c * 32 + e + u;
-                        const int q = q0 + col;
-                        const bool valid = key_ok && q < N && (!p.causal || key <= q);
-                        const float x = fmaf(__uint_as_float(sr[e + u]), sl2, -lv[col]);
-                        const float pr = valid ? ex2(x) : 0.f;
-                        pv[u] = pr;
-                        dsv[u] = pr * (__uint_as_float(dr[e + u]) - dv[col]);
+                    for (int e = 0; e < 32; ++e) {
+                        const int q = q0 + c * 32 + e;
+                        if (!(key_ok && q < N && (!p.causal || key <= q))) sr[e] = __float_as_uint(-INFINITY);
                     }
-                    pp[e >> 1] = pack_bf16(pv[0], pv[1]);
-                    dp[e >> 1] = pack_bf16(dsv[0], dsv[1]);
+                }
+                uint32_t pp[16], dp[16];
+                const float4 *l4 = reinterpret_cast<const float4 *>(lv + c * 32);
+                const float4 *d4 = reinterpret_cast<const float4 *>(dv + c * 32);
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 lq = l4[e >> 2], dq = d4[e >> 2];
+                    const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl22,
+                                                 make_float2(-lq.x, -lq.y));
+                    const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])),
+                                                 sl22, make_float2(-lq.z, -lq.w));
+                    const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y)), p1 = make_float2(ex2(x1.x), ex2(x1.y));
+                    const float2 g0 = __fmul2_rn(p0, make_float2(__uint_as_float(dr[e]) - dq.x, __uint_as_float(dr[e + 1]) - dq.y));
+                    const float2 g1 =
+                        __fmul2_rn(p1, make_float2(__uint_as_float(dr[e + 2]) - dq.z, __uint_as_float(dr[e + 3]) - dq.w));
+                    pp[e >> 1] = pack_bf16(p0.x, p0.y);
+                    pp[(e >> 1) + 1] = pack_bf16(p1.x, p1.y);
+                    dp[e >> 1] = pack_bf16(g0.x, g0.y);
+                    dp[(e >> 1) + 1] = pack_bf16(g1.x, g1.y);
                 }
                 // packed columns 16c..16c+15 lie in chunks already read
                 tmem_st16(tmem + lane_off + kColS + c * 16, pp);
@@ -539,6 +551,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
             __syncwarp();
             const int kb = n * BT;
+            // masking only where the key tile touches key_len, the diagonal or the row tail
+            const bool need_mask = kb + BT > klen || q0 + BT > N || (p.causal && kb + BT - 1 > q0);
+            const float2 sl22 = make_float2(sl2, sl2), nl2 = make_float2(-lrow, -lrow);
+            const float2 ndr2 = make_float2(-drow, -drow);
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t sr[32], dr[32];
@@ -547,18 +563,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_wait_ld();
                 reg_fence(sr);
                 reg_fence(dr);
+                if (need_mask) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int key = kb + c * 32 + e;
+                        if (!(q < N && key < klen && (!p.causal || key <= q))) sr[e] = __float_as_uint(-INFINITY);
+                    }
+                }
                 uint32_t dp[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    float dsv[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int key = kb + c * 32 + e + u;
-                        const bool valid = q < N && key < klen && (!p.causal || key <= q);
-                        const float pr = valid ? ex2(fmaf(__uint_as_float(sr[e + u]), sl2, -lrow)) : 0.f;
-                        dsv[u] = pr * (__uint_as_float(dr[e + u]) - drow);
-                    }
-                    dp[e >> 1] = pack_bf16(dsv[0], dsv[1]);
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl22, nl2);
+                    const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+                    const float2 g = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), ndr2));
+                    dp[e >> 1] = pack_bf16(g.x, g.y);
                 }
                 tmem_st16(tmem + lane_off + kColDP + c * 16, dp);
             }

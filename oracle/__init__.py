@@ -25,5 +25,7 @@ from .oracle import (  # noqa: F401
     decode_paged,
     sdpa_forward_f64,
     sdpa_backward,
+    e4m3_to_f64,
+    sdpa_forward_e4m3,
     max_threads,
 )

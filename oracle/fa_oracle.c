@@ -30,6 +30,12 @@
  *    and online softmax; section 2.2 and Exercise 1: the online recurrence
  *    d_j = d_{j-1} exp(m_{j-1} - m_j) + exp(x_j - m_j).
  *
+ * FP8 inputs (the e4m3 variant of the forward) are decoded exactly by
+ * oracle_e4m3_to_f64, written from the OCP 8-bit floating-point format
+ * definition (E4M3: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ * bits, subnormals at exponent 0, no infinities, S.1111.111 = NaN); the
+ * attention itself then runs through oracle_sdpa_forward_f64.
+ *
  * Everything is float64.  Inputs arrive as bfloat16 bit patterns (the same
  * bits the GPU receives) and are widened exactly: a bfloat16 value is the top
  * 16 bits of an IEEE-754 binary32 value.
@@ -501,6 +507,26 @@ int oracle_sdpa_backward(const double *Q, const double *K, const double *V, cons
         free(s); free(pr); free(dp); free(o);
     }
     return bad ? -1 : 0;
+}
+
+/* E4M3 (OCP 8-bit floating point) to float64, exactly:
+ *   exponent field e in 1..15: (-1)^s * 2^(e-7) * (1 + m/8)
+ *   e = 0 (subnormal):         (-1)^s * 2^(-6) * (m/8)
+ *   e = 15 and m = 7:          NaN (the format has no infinities) */
+void oracle_e4m3_to_f64(const uint8_t *x, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const unsigned b = x[i];
+        const int sgn = (b >> 7) & 1, e = (b >> 3) & 15, m = b & 7;
+        double v;
+        if (e == 15 && m == 7)
+            v = NAN;
+        else if (e == 0)
+            v = ldexp((double)m / 8.0, -6);
+        else
+            v = ldexp(1.0 + (double)m / 8.0, e - 7);
+        out[i] = sgn ? -v : v;
+    }
 }
 
 int oracle_max_threads(void)

@@ -90,6 +90,7 @@ def _load():
                                              ctypes.c_int, ctypes.c_int, ctypes.c_double, _i32p,
                                              _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
         lib.oracle_sdpa_backward.restype = ctypes.c_int
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.POINTER(ctypes.c_uint8), ctypes.c_int64, _dp]
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -393,3 +394,26 @@ def sdpa_backward(Q, K, V, dO, causal=False, scale=None, key_len=None, magnitude
     if magnitudes:
         out.update(M_dV=mag[0], M_dK=mag[1], M_dQ=mag[2])
     return out
+
+
+def e4m3_to_f64(x):
+    """Exact float64 values of E4M3 codes (a uint8 numpy array or a torch float8_e4m3fn/uint8 tensor)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            t = x.detach().cpu().contiguous()
+            if t.dtype != torch.uint8:
+                t = t.view(torch.uint8)
+            x = t.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.uint8))
+    out = np.empty(a.shape, dtype=np.float64)
+    _load().oracle_e4m3_to_f64(a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), a.size, _ptr(out, _dp))
+    return out
+
+
+def sdpa_forward_e4m3(Q8, K8, V8, causal=False, scale=None, key_len=None):
+    """Exact attention on E4M3 inputs (codes decoded exactly): O [B,H,N,d], L [B,H,N]."""
+    return sdpa_forward_f64(e4m3_to_f64(Q8), e4m3_to_f64(K8), e4m3_to_f64(V8), causal=causal, scale=scale,
+                            key_len=key_len)

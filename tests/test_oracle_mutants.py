@@ -2,8 +2,9 @@
 
 Each case plants one mistake in a temporary copy of the oracle's C source (a
 dropped rescale term, a flipped sign, a wrong operand or index, a missing
-scale or log), builds it, and runs the pin suites (tests/test_oracle_pins.py
-and tests/test_oracle_backward_pins.py) against that copy in a subprocess.  The pin suite must fail for every mutant.  The
+scale or log), builds it, and runs the pin suites (tests/test_oracle_pins.py,
+tests/test_oracle_backward_pins.py and tests/test_oracle_fp8_pins.py) against
+that copy in a subprocess.  The pin suite must fail for every mutant.  The
 committed oracle itself is never modified.
 """
 import os
@@ -46,6 +47,10 @@ MUTANTS = {
     "bwd_dK_no_scale": ("dKb[(size_t)j * d + c] += scale * ds * q[c];", "dKb[(size_t)j * d + c] += ds * q[c];"),
     "bwd_dQ_uses_values": ("dq[c] += scale * ds * kb[(size_t)j * d + c];",
                            "dq[c] += scale * ds * vb[(size_t)j * d + c];"),
+    # E4M3 decoding
+    "e4m3_bias_off_by_one": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "e4m3_subnormal_scale": ("v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);"),
+    "e4m3_no_nan": ("if (e == 15 && m == 7)", "if (e == 16)"),
 }
 
 
@@ -64,6 +69,7 @@ def test_pins_reject_mutant(name, tmp_path):
     env = dict(os.environ, FA_ORACLE_LIB_OVERRIDE=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_backward_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_backward_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_fp8_pins.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pin suite passed with mutant {name}:\n{r.stdout[-2000:]}"

@@ -10,6 +10,7 @@ PyTorch fallback, and the calls raise if ``libfa.so`` is missing.
     fa_decode(q, Kcache, Vcache, seqlens, num_splits=0, ...)   -> (O, L)
     fa_decode_paged(q, Kpool, Vpool, block_table, seqlens, ...) -> (O, L)
     fa_backward(Q, K, V, O, dO, L, causal=False, ...)           -> (dQ, dK, dV)
+    fa_forward_fp8(Q8, K8, V8, causal=False, ...)               -> (O, L)
 """
 from __future__ import annotations
 
@@ -17,7 +18,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["fa_forward", "fa_backward", "fa_backward_workspace_bytes", "fa_decode", "fa_decode_paged", "fa_decode_plan", "fa_decode_workspace_bytes",
+__all__ = ["fa_forward", "fa_forward_fp8", "fa_backward", "fa_backward_workspace_bytes", "fa_decode", "fa_decode_paged", "fa_decode_plan", "fa_decode_workspace_bytes",
            "fa_device_error", "FaError", "library", "library_path", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -62,6 +63,11 @@ def library():
         lib.fa_backward.restype = _i
         lib.fa_backward_workspace_bytes.argtypes = [_i, _i, _i, _i]
         lib.fa_backward_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_forward_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp,
+                                        ctypes.c_size_t, _vp]
+        lib.fa_forward_fp8.restype = _i
+        lib.fa_forward_fp8_workspace_bytes.argtypes = [_i, _i, _i, _i]
+        lib.fa_forward_fp8_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                                          ctypes.c_float, _i, _vp, ctypes.c_size_t, _vp]
         lib.fa_decode_paged.restype = _i
@@ -148,6 +154,46 @@ def fa_forward(Q, K, V, causal=False, scale=None, key_len=None, out=None, lse=No
     if st != 0:
         raise FaError(st, "fa_forward")
     return out, lse
+
+
+def _check_e4m3(name, t):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError(f"{name} must be a CUDA float8_e4m3fn (or uint8 E4M3 code) tensor")
+    if t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 4-D tensor")
+
+
+def fa_forward_fp8(Q8, K8, V8, causal=False, scale=None, key_len=None, out=None, lse=None, return_lse=True,
+                   workspace=None, stream=None):
+    """Exact attention over E4M3 inputs [B, H, N, 128]; returns (O bf16, L float32)."""
+    torch = _torch()
+    for n, t in (("Q8", Q8), ("K8", K8), ("V8", V8)):
+        _check_e4m3(n, t)
+        if t.shape != Q8.shape:
+            raise ValueError(f"{n} must have the shape of Q8")
+    B, H, N, d = Q8.shape
+    if out is None:
+        out = torch.empty((B, H, N, d), device=Q8.device, dtype=torch.bfloat16)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), device=Q8.device, dtype=torch.float32)
+    if key_len is not None:
+        if key_len.dtype != torch.int32 or not key_len.is_cuda or key_len.numel() != B:
+            raise TypeError("key_len must be a CUDA int32 tensor with B entries")
+        key_len = key_len.contiguous()
+    need = library().fa_forward_fp8_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), device=Q8.device, dtype=torch.uint8)
+    st = library().fa_forward_fp8(_ptr(Q8), _ptr(K8), _ptr(V8), _ptr(out), _ptr(lse), B, H, N, d,
+                                  int(bool(causal)), float(scale) if scale is not None else 0.0, _ptr(key_len),
+                                  _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, "fa_forward_fp8")
+    return out, lse
+
+
+def fa_forward_fp8_workspace_bytes(B, H, N, d):
+    return int(library().fa_forward_fp8_workspace_bytes(B, H, N, d))
 
 
 def fa_backward_workspace_bytes(B, H, N, d):

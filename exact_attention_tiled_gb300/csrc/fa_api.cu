@@ -328,6 +328,52 @@ fa_status fa_decode_paged(const void *q, const void *Kpool, const void *Vpool, c
                        num_splits, workspace, workspace_bytes, paged, static_cast<cudaStream_t>(stream));
 }
 
+size_t fa_forward_fp8_workspace_bytes(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || B > 65535 || H > 65535 || d != 128) return 0;
+    return align256(static_cast<size_t>(B) * H * N * d * 2);
+}
+
+fa_status fa_forward_fp8(const void *Q8, const void *K8, const void *V8, void *O, float *L, int B, int H,
+                         int N, int d, int causal, float scale, const int32_t *key_len, void *workspace,
+                         size_t workspace_bytes, fa_stream_t stream) {
+    if (!Q8 || !K8 || !V8 || !O) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned(Q8, 16) || !aligned(K8, 16) || !aligned(V8, 16) || !aligned(O, 16) || (L && !aligned(L, 4)) ||
+        (key_len && !aligned(key_len, 4)))
+        return FA_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H * N > (1ll << 40)) return FA_ERR_UNSUPPORTED;
+    if (!(std::isfinite(scale))) return FA_ERR_INVALID_ARG;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(d));
+    const size_t need = fa_forward_fp8_workspace_bytes(B, H, N, d);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return FA_ERR_WORKSPACE;
+
+    unsigned *err = nullptr;
+    fa_status s = error_word(&err);
+    if (s != FA_OK) return s;
+    const long long n = static_cast<long long>(B) * H * N * d;
+    if (launch_e4m3_to_bf16(V8, workspace, n, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+
+    PrefillParams p;
+    std::memset(&p, 0, sizeof p);
+    p.Q = Q8;
+    p.K = K8;
+    p.V = workspace;
+    p.O = O;
+    p.L = L;
+    p.key_len = key_len;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.causal = causal;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+    p.qk_e4m3 = 1;
+    if (launch_prefill(p, d, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
 size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 1 || B > 65535 || H > 65535 || (d != 64 && d != 128)) return 0;
     return align256(static_cast<size_t>(B) * H * N * sizeof(float));

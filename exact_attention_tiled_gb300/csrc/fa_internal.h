@@ -48,9 +48,12 @@ struct PrefillParams {
     int causal;
     float scale_log2;       // scale * log2(e)
     unsigned *err;
+    int qk_e4m3;            // Q and K are E4M3 [B, H, N, d] (d = 128); V stays bf16
 };
 
 cudaError_t launch_prefill(const PrefillParams &p, int d, cudaStream_t stream);
+// E4M3 -> bf16 (exact) for n elements; n a multiple of 8, both pointers 16-byte aligned.
+cudaError_t launch_e4m3_to_bf16(const void *src, void *dst, long long n, cudaStream_t stream);
 
 // ------------------------------------------------------------------ backward
 struct BwdParams {

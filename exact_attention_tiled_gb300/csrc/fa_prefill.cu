@@ -47,6 +47,7 @@
 // as soon as it sees S_t(j+1).
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -166,10 +167,17 @@ __device__ __forceinline__ int item_of_round(int r, int G, int c) {
     return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
-template <int D>
+template <int D, bool QK8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ TmapSet tm, const PrefillParams p, int num_items, int npairs, int upb) {
     using C = Cfg<D>;
+    // QK8: Q and K are E4M3 (one byte per element) and S = Q K^T runs as
+    // tcgen05.mma kind::f8f6f4; V, P and O stay bf16.  A row of an FP8 tile
+    // at d = 128 is one 128-byte swizzle atom.
+    constexpr int kQKBlocks = QK8 ? D / 128 : C::kColBlocks;      // 128-byte column blocks
+    constexpr int kQKBlockElems = QK8 ? 128 : 64;
+    constexpr uint32_t kQTileBytes = QK8 ? BM * D : C::kTileBytes;
+    constexpr uint32_t kKTileBytes = QK8 ? BN * D : C::kTileBytes;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzled tiles need 1024-byte aligned bases.
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -248,23 +256,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int t = 0; t < 2; ++t)
 #pragma unroll
-                            for (int cb = 0; cb < C::kColBlocks; ++cb)
-                                tma_prefetch_3d(&tm.q, cb * 64, nx.row0[t], nx.bh);
+                            for (int cb = 0; cb < kQKBlocks; ++cb)
+                                tma_prefetch_3d(&tm.q, cb * kQKBlockElems, nx.row0[t], nx.bh);
                     }
                     // Q smem is free once the previous item's last S MMA completed
                     if (qi > 0 && !wait_or_abort(bar_q_free, (qi - 1) & 1, p.err, kSiteQ, abort_flag)) break;
-                    mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
+                    mbar_arrive_expect_tx(bar_q, 2 * kQTileBytes);
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
 #pragma unroll
-                        for (int cb = 0; cb < C::kColBlocks; ++cb)
-                            tma_load_3d(q_smem + t * C::kTileBytes + cb * (BM * 128), &tm.q, cb * 64, it.row0[t],
+                        for (int cb = 0; cb < kQKBlocks; ++cb)
+                            tma_load_3d(q_smem + t * C::kTileBytes + cb * (BM * 128), &tm.q, cb * kQKBlockElems,
+                                        it.row0[t],
                                         it.bh, bar_q, pol_q);
                     ++qi;
                     for (int j = 0; j < kPrefetchTiles && j < it.ntot; ++j)
 #pragma unroll
                         for (int cb = 0; cb < C::kColBlocks; ++cb) {
-                            tma_prefetch_3d(&tm.k, cb * 64, j * BN, it.bh);
+                            if (cb < kQKBlocks) tma_prefetch_3d(&tm.k, cb * kQKBlockElems, j * BN, it.bh);
                             tma_prefetch_3d(&tm.v, cb * 64, j * BN, it.bh);
                         }
                     for (int j = 0; ok && j < it.ntot; ++j) {
@@ -276,19 +285,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 ok = false;
                                 break;
                             }
-                            mbar_arrive_expect_tx(bar_kv_full(s), C::kTileBytes);
+                            mbar_arrive_expect_tx(bar_kv_full(s), kv ? C::kTileBytes : kKTileBytes);
                             const CUtensorMap *map = kv ? &tm.v : &tm.k;
+                            const int nblk = kv ? C::kColBlocks : kQKBlocks;
+                            const int belems = kv ? 64 : kQKBlockElems;
 #pragma unroll
                             for (int cb = 0; cb < C::kColBlocks; ++cb)
-                                tma_load_3d(ring + s * C::kTileBytes + cb * (BN * 128), map, cb * 64, j * BN,
-                                            it.bh, bar_kv_full(s), pol_kv);
+                                if (cb < nblk)
+                                    tma_load_3d(ring + s * C::kTileBytes + cb * (BN * 128), map, cb * belems,
+                                                j * BN, it.bh, bar_kv_full(s), pol_kv);
                             // Warm L2 with the same tensor's tile kPrefetchTiles steps
                             // ahead: the CTAs of one head walk the KV tiles in step, so
                             // a tile's first touch would otherwise stall them on DRAM.
                             if (j + kPrefetchTiles < it.ntot)
 #pragma unroll
                                 for (int cb = 0; cb < C::kColBlocks; ++cb)
-                                    tma_prefetch_3d(map, cb * 64, (j + kPrefetchTiles) * BN, it.bh);
+                                    if (cb < nblk) tma_prefetch_3d(map, cb * belems, (j + kPrefetchTiles) * BN, it.bh);
                             ++g;
                         }
                     }
@@ -306,16 +318,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool issued_any = false;
             {
                 constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
+                constexpr uint32_t idesc_s8 = idesc_e4m3_f32(BM, BN);
                 constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);
                 // A descriptor advanced by a byte offset: the start-address
                 // field holds address >> 4 and never carries (SMEM < 256 KB).
                 auto issue_s = [&](int t, uint32_t kslot) {
                     const uint64_t qd = sdesc_sw128(q_smem + t * C::kTileBytes, 16, 1024);
                     const uint64_t kd = sdesc_sw128(kslot, 16, 1024);
+                    if constexpr (QK8) {
+                        // K = 32 one-byte elements per instruction: 32-byte steps along the atom
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
-                        mma_ss_warp(tmem + t * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 32; ++kk) {
+                            const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+                            mma_ss_f8_warp(tmem + t * 128, qd + off, kd + off, idesc_s8, kk > 0 ? 1u : 0u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+                            mma_ss_warp(tmem + t * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+                        }
                     }
                 };
                 auto issue_pv = [&](int t, uint32_t vslot, int j) {
@@ -611,23 +633,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
-template <int D>
+template <int D, bool QK8 = false>
 cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
     TmapSet tm;
     std::memset(&tm, 0, sizeof tm);
     const int BH = p.B * p.H;
-    if (!make_map(&tm.q, p.Q, BH, p.N, D) || !make_map(&tm.k, p.K, BH, p.N, D) ||
-        !make_map(&tm.v, p.V, BH, p.N, D))
-        return cudaErrorInvalidValue;
+    const bool maps = QK8 ? make_map_u8(&tm.q, p.Q, BH, p.N, D) && make_map_u8(&tm.k, p.K, BH, p.N, D)
+                          : make_map(&tm.q, p.Q, BH, p.N, D) && make_map(&tm.k, p.K, BH, p.N, D);
+    if (!maps || !make_map(&tm.v, p.V, BH, p.N, D)) return cudaErrorInvalidValue;
     const int smem = Cfg<D>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, QK8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // setmaxnreg.inc only completes when the registers it asks for exist in
     // the block's launch allocation: refuse to launch a build where they do not.
     static int regs_ok = -1;
     if (regs_ok < 0) {
         cudaFuncAttributes fa_attr;
-        e = cudaFuncGetAttributes(&fa_attr, prefill_kernel<D>);
+        e = cudaFuncGetAttributes(&fa_attr, prefill_kernel<D, QK8>);
         if (e != cudaSuccess) return e;
         const long long have = static_cast<long long>(fa_attr.numRegs) * kThreads;
         const long long want = 2ll * 128 * kRegsSoftmax + 128ll * kRegsAux;
@@ -657,13 +679,45 @@ cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
     long long upb = p.causal ? BH : kL2BlockBytes / (kv_unit > 0 ? kv_unit : 1);
     if (upb < 1) upb = 1;
     if (upb > static_cast<long long>(BH)) upb = BH;
-    prefill_kernel<D><<<grid, kThreads, smem, stream>>>(tm, p, static_cast<int>(items), npairs, static_cast<int>(upb));
+    prefill_kernel<D, QK8><<<grid, kThreads, smem, stream>>>(tm, p, static_cast<int>(items), npairs,
+                                                              static_cast<int>(upb));
     return cudaGetLastError();
+}
+
+// E4M3 -> bf16, 8 elements per thread.  Every E4M3 value (|x| <= 448, down to
+// 2^-9) is a bf16 value, so the widening is exact.
+__global__ void __launch_bounds__(256) e4m3_to_bf16_kernel(const uint2 *src, uint4 *dst, long long n8) {
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const uint2 v = src[i];
+    const uint32_t w[2] = {v.x, v.y};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint16_t pair = static_cast<uint16_t>(w[k >> 1] >> (16 * (k & 1)));
+        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair), __NV_E4M3);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+        o[k] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace
 
+cudaError_t launch_e4m3_to_bf16(const void *src, void *dst, long long n, cudaStream_t stream) {
+    if (n % 8 != 0) return cudaErrorInvalidValue;
+    const long long n8 = n / 8;
+    const long long blocks = (n8 + 255) / 256;
+    if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+    if (blocks == 0) return cudaSuccess;
+    e4m3_to_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<const uint2 *>(src),
+                                                                          static_cast<uint4 *>(dst), n8);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_prefill(const PrefillParams &p, int d, cudaStream_t stream) {
+    if (p.qk_e4m3) return d == 128 ? launch_d<128, true>(p, stream) : cudaErrorInvalidValue;
     return d == 128 ? launch_d<128>(p, stream) : launch_d<64>(p, stream);
 }
 

@@ -93,6 +93,33 @@ FA_API fa_status fa_forward(const void *Q, const void *K, const void *V, void *O
                      const int32_t *key_len, fa_stream_t stream);
 
 /*
+ * fa_forward_fp8 -- fa_forward with FP8 (E4M3) inputs.  ("Infra: Flash
+ * Attention", "FlashAttention-3": FA3 explores FP8 and its quantisation error
+ * has to be evaluated on its own.)  The attention computed is exactly
+ * fa_forward's over the E4M3 values of Q, K and V:
+ *   S = Q K^T * scale runs on the FP8 tensor cores (tcgen05.mma kind::f8f6f4,
+ *   E4M3 x E4M3, fp32 accumulation: every product is exact);
+ *   V is widened to bf16 (exact for every E4M3 value) into `workspace`, and
+ *   P V runs as in fa_forward (P rounded to bf16, fp32 accumulation).
+ * So the kernel's rounding is that of fa_forward on the same values; the
+ * error of quantising real-valued inputs to E4M3 is the caller's.
+ *
+ *   Q8, K8, V8  E4M3 codes (one byte each) [B, H, N, d], contiguous; d = 128
+ *               (others: FA_ERR_UNSUPPORTED).  No scale factors: the codes are
+ *               the values.
+ *   O, L, B, H, N, causal, scale, key_len: as in fa_forward.
+ *   workspace   device scratch of at least fa_forward_fp8_workspace_bytes()
+ *               bytes, 256-byte aligned (the bf16 copy of V).
+ */
+FA_API fa_status fa_forward_fp8(const void *Q8, const void *K8, const void *V8, void *O, float *L,
+                                int B, int H, int N, int d, int causal, float scale,
+                                const int32_t *key_len, void *workspace, size_t workspace_bytes,
+                                fa_stream_t stream);
+
+/* Workspace bytes fa_forward_fp8 needs (0 for arguments it would reject). */
+FA_API size_t fa_forward_fp8_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * fa_backward -- gradients of exact attention ("Infra: Flash Attention",
  * sections "Backward and recomputation" and "Blocked gradient computation";
  * CMU 10-423 Lecture 18 notes, 5.3).  With S = scale Q K^T (masked as in

@@ -218,3 +218,20 @@ def test_backward_rejects_bad_arguments_before_cuda(lib):
     assert _bwd(lib, wsb=16) == 4
     assert lib.fa_backward_workspace_bytes(2, 3, 1000, 128) == (2 * 3 * 1000 * 4 + 255) // 256 * 256
     assert lib.fa_backward_workspace_bytes(2, 3, 1000, 96) == 0
+
+
+def test_forward_fp8_rejects_bad_arguments_before_cuda(lib):
+    def f8(**kw):
+        a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, L=None, B=1, H=2, N=256, d=128, causal=0, scale=0.0, kl=None,
+                 ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return lib.fa_forward_fp8(a["Q"], a["K"], a["V"], a["O"], a["L"], a["B"], a["H"], a["N"], a["d"],
+                                  a["causal"], ctypes.c_float(a["scale"]), a["kl"], a["ws"], a["wsb"], None)
+    assert f8(Q=None) == 1
+    assert f8(V=FAKE + 4) == 1
+    assert f8(N=0) == 1
+    assert f8(d=64) == 2
+    assert f8(ws=None) == 4
+    assert f8(wsb=1024) == 4
+    assert lib.fa_forward_fp8_workspace_bytes(1, 2, 300, 128) == (2 * 300 * 128 * 2 + 255) // 256 * 256
+    assert lib.fa_forward_fp8_workspace_bytes(1, 2, 300, 64) == 0

@@ -42,7 +42,8 @@ namespace fa {
 namespace {
 
 constexpr int BT = 128;              // rows of a query or key tile (MMA M and N)
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 256;     // dQ kernel: producer, MMA, 2 idle warps, one compute warpgroup
+constexpr int kDkdvThreads = 384;    // dK/dV kernel: two compute warpgroups (query columns 0-63 / 64-127)
 constexpr int kProd = 0, kMma = 1, kFirstCompute = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *O, co
 // under causal masking: key tile j meets the query tiles i >= j).
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDkdvThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -153,6 +154,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
     auto bar_empty = [&](int s) { return bars + 8u * (3 + s); };
     const uint32_t bar_st = bars + 8u * 5, bar_ps = bars + 8u * 6, bar_done = bars + 8u * 7;
+    // the first compute warpgroup has read score columns 0-63, which the second
+    // warpgroup's packed P^T / dS^T (query columns 64-127) then overwrite
+    const uint32_t bar_half = bars + 8u * 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
@@ -175,8 +179,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar_empty(s), 1);
         }
         mbar_init(bar_st, 1);
-        mbar_init(bar_ps, 4);
+        mbar_init(bar_ps, 8);
         mbar_init(bar_done, 1);
+        mbar_init(bar_half, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -209,6 +214,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int n = 0; n < nsteps && ok; ++n) {
                 const int s = n % C::kStages;
                 const int i = i_lo + n;
+                // L_i * log2(e) and D_i of this query tile, loaded before the stage
+                // wait so their latency hides behind it (rows past N: never used)
+                float lreg[BT / 32], dreg[BT / 32];
+#pragma unroll
+                for (int e = 0; e < BT / 32; ++e) {
+                    const int q = i * BT + e * 32 + lane;
+                    const size_t idx = static_cast<size_t>(bh) * N + (q < N ? q : 0);
+                    lreg[e] = p.L[idx] * kLog2e;
+                    dreg[e] = p.Dvec[idx];
+                }
                 if (n >= C::kStages)
                     ok = __all_sync(0xffffffffu, wait_abort(bar_empty(s), ((n / C::kStages) - 1) & 1, p.err,
                                                              kSiteBwEmpty, abort_flag));
@@ -222,14 +237,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tma_load_3d(do_stage(s) + cb * (BT * 128), &tm.dO, cb * 64, i * BT, bh, bar_full(s), pol);
                     }
                 }
-                // L_i * log2(e) and D_i of this query tile (rows past N: never used)
                 float *lv = vec + s * 2 * BT;
 #pragma unroll
                 for (int e = 0; e < BT / 32; ++e) {
-                    const int q = i * BT + e * 32 + lane;
-                    const size_t idx = static_cast<size_t>(bh) * N + q;
-                    lv[e * 32 + lane] = q < N ? p.L[idx] * kLog2e : 0.f;
-                    lv[BT + e * 32 + lane] = q < N ? p.Dvec[idx] : 0.f;
+                    lv[e * 32 + lane] = lreg[e];
+                    lv[BT + e * 32 + lane] = dreg[e];
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_full(s));
@@ -291,13 +303,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __syncwarp();
         }
     } else if (warp >= kFirstCompute) {
-        // ================================================= compute warpgroup
+        // ================================================= compute warpgroups
+        // warpgroup h handles query columns [64h, 64h + 64) of every step, one
+        // thread per key row (TMEM lane)
+        const int h = (warp - kFirstCompute) >> 2;
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;      // key row of the tile
         const int key = key0 + r;
         const bool key_ok = key < klen;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const float sl2 = p.scale_log2;
+        const float2 sl22 = make_float2(sl2, sl2);
         bool ok = true;
         for (int n = 0; n < nsteps && ok; ++n) {
             const int s = n % C::kStages;
@@ -313,15 +329,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float *dv = lv + BT;              // D_i
             // masking only where the tile touches key_len, the sequence end or the diagonal
             const bool need_mask = key0 + BT > klen || q0 + BT > N || (p.causal && key0 + BT - 1 > q0);
-            const float2 sl22 = make_float2(sl2, sl2);
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_off + kColS + c * 32, sr);
-                tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
-                tmem_wait_ld();
-                reg_fence(sr);
-                reg_fence(dr);
+            // P^T and dS^T of the 32-column chunk c from its S^T and dP^T values
+            auto chunk = [&](int c, uint32_t (&sr)[32], const uint32_t (&dr)[32], uint32_t (&pp)[16],
+                             uint32_t (&dp)[16]) {
                 if (need_mask) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
@@ -329,7 +339,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         if (!(key_ok && q < N && (!p.causal || key <= q))) sr[e] = __float_as_uint(-INFINITY);
                     }
                 }
-                uint32_t pp[16], dp[16];
                 const float4 *l4 = reinterpret_cast<const float4 *>(lv + c * 32);
                 const float4 *d4 = reinterpret_cast<const float4 *>(dv + c * 32);
 #pragma unroll
@@ -340,7 +349,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])),
                                                  sl22, make_float2(-lq.z, -lq.w));
                     const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y)), p1 = make_float2(ex2(x1.x), ex2(x1.y));
-                    const float2 g0 = __fmul2_rn(p0, make_float2(__uint_as_float(dr[e]) - dq.x, __uint_as_float(dr[e + 1]) - dq.y));
+                    const float2 g0 =
+                        __fmul2_rn(p0, make_float2(__uint_as_float(dr[e]) - dq.x, __uint_as_float(dr[e + 1]) - dq.y));
                     const float2 g1 =
                         __fmul2_rn(p1, make_float2(__uint_as_float(dr[e + 2]) - dq.z, __uint_as_float(dr[e + 3]) - dq.w));
                     pp[e >> 1] = pack_bf16(p0.x, p0.y);
@@ -348,9 +358,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     dp[e >> 1] = pack_bf16(g0.x, g0.y);
                     dp[(e >> 1) + 1] = pack_bf16(g1.x, g1.y);
                 }
-                // packed columns 16c..16c+15 lie in chunks already read
-                tmem_st16(tmem + lane_off + kColS + c * 16, pp);
-                tmem_st16(tmem + lane_off + kColDP + c * 16, dp);
+            };
+            if (h == 0) {
+                // read columns 0-63 of S^T and dP^T first: the packed results of both
+                // warpgroups land in them
+                uint32_t s0[32], s1[32], d0[32], d1[32];
+                tmem_ld32(tmem + lane_off + kColS, s0);
+                tmem_ld32(tmem + lane_off + kColS + 32, s1);
+                tmem_ld32(tmem + lane_off + kColDP, d0);
+                tmem_ld32(tmem + lane_off + kColDP + 32, d1);
+                tmem_wait_ld();
+                reg_fence(s0);
+                reg_fence(s1);
+                reg_fence(d0);
+                reg_fence(d1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_half);
+                uint32_t pp[16], dp[16];
+                chunk(0, s0, d0, pp, dp);
+                tmem_st16(tmem + lane_off + kColS, pp);
+                tmem_st16(tmem + lane_off + kColDP, dp);
+                chunk(1, s1, d1, pp, dp);
+                tmem_st16(tmem + lane_off + kColS + 16, pp);
+                tmem_st16(tmem + lane_off + kColDP + 16, dp);
+            } else {
+#pragma unroll 1
+                for (int c = 2; c < 4; ++c) {
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32(tmem + lane_off + kColS + c * 32, sr);
+                    tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
+                    tmem_wait_ld();
+                    reg_fence(sr);
+                    reg_fence(dr);
+                    uint32_t pp[16], dp[16];
+                    chunk(c, sr, dr, pp, dp);
+                    if (c == 2) {   // columns 32-63 are overwritten below: wait until they were read
+                        ok = wait_abort_warp(bar_half, n & 1, p.err, kSiteBwP, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    tmem_st16(tmem + lane_off + kColS + c * 16, pp);
+                    tmem_st16(tmem + lane_off + kColDP + c * 16, dp);
+                }
+                if (!ok) break;
             }
             tmem_wait_st();
             tc_fence_before();
@@ -366,8 +417,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // tcgen05.ld is warp-collective: every lane loads, only rows < N store
         if (ok) {
             const size_t row = (static_cast<size_t>(bh) * N + (key < N ? key : 0)) * D;
-#pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
+            {
+                const int which = h;   // warpgroup 0 writes dV, warpgroup 1 dK
                 __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(which ? p.dK : p.dV) + row;
                 const float mul = which ? p.scale : 1.f;
 #pragma unroll 1
@@ -653,7 +704,7 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int T = (p.N + BT - 1) / BT;
     const dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(T));
-    bwd_dkdv_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tm, p);
+    bwd_dkdv_kernel<D><<<grid, kDkdvThreads, smem, stream>>>(tm, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     bwd_dq_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tm, p);

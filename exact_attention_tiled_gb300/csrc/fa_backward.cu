@@ -42,8 +42,9 @@ namespace fa {
 namespace {
 
 constexpr int BT = 128;              // rows of a query or key tile (MMA M and N)
-constexpr int kBwdThreads = 256;     // dQ kernel: producer, MMA, 2 idle warps, one compute warpgroup
-constexpr int kDkdvThreads = 384;    // dK/dV kernel: two compute warpgroups (query columns 0-63 / 64-127)
+// warp 0 producer, warp 1 MMA, warps 2-3 idle, two compute warpgroups: the dK/dV
+// kernel splits each step's query columns 0-63 / 64-127, the dQ kernel its key columns
+constexpr int kBwdThreads = 384;
 constexpr int kProd = 0, kMma = 1, kFirstCompute = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *O, co
 // under causal masking: key tile j meets the query tiles i >= j).
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kDkdvThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -474,6 +475,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
     auto bar_empty = [&](int s) { return bars + 8u * (3 + s); };
     const uint32_t bar_st = bars + 8u * 5, bar_ps = bars + 8u * 6, bar_done = bars + 8u * 7;
+    const uint32_t bar_half = bars + 8u * 8;   // dP columns 0-63 read by the first warpgroup
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
@@ -497,8 +499,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar_empty(s), 1);
         }
         mbar_init(bar_st, 1);
-        mbar_init(bar_ps, 4);
+        mbar_init(bar_ps, 8);
         mbar_init(bar_done, 1);
+        mbar_init(bar_half, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -585,6 +588,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __syncwarp();
         }
     } else if (warp >= kFirstCompute) {
+        // warpgroup h handles key columns [64h, 64h + 64) of every step, one thread per query row
+        const int h = (warp - kFirstCompute) >> 2;
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const int q = q0 + r;
@@ -595,6 +600,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             lrow = p.L[static_cast<size_t>(bh) * N + q] * kLog2e;
             drow = p.Dvec[static_cast<size_t>(bh) * N + q];
         }
+        const float2 sl22 = make_float2(sl2, sl2), nl2 = make_float2(-lrow, -lrow);
+        const float2 ndr2 = make_float2(-drow, -drow);
         bool ok = true;
         for (int n = 0; n < nsteps && ok; ++n) {
             ok = wait_abort_warp(bar_st, n & 1, p.err, kSiteBwS, abort_flag);
@@ -604,16 +611,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int kb = n * BT;
             // masking only where the key tile touches key_len, the diagonal or the row tail
             const bool need_mask = kb + BT > klen || q0 + BT > N || (p.causal && kb + BT - 1 > q0);
-            const float2 sl22 = make_float2(sl2, sl2), nl2 = make_float2(-lrow, -lrow);
-            const float2 ndr2 = make_float2(-drow, -drow);
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_off + kColS + c * 32, sr);
-                tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
-                tmem_wait_ld();
-                reg_fence(sr);
-                reg_fence(dr);
+            // dS of the 32-key chunk c (packed bf16 pairs) from its S and dP values
+            auto chunk = [&](int c, uint32_t (&sr)[32], const uint32_t (&dr)[32], uint32_t (&dp)[16]) {
                 if (need_mask) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
@@ -621,15 +620,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         if (!(q < N && key < klen && (!p.causal || key <= q))) sr[e] = __float_as_uint(-INFINITY);
                     }
                 }
-                uint32_t dp[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl22, nl2);
                     const float2 pr = make_float2(ex2(x.x), ex2(x.y));
-                    const float2 g = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), ndr2));
+                    const float2 g =
+                        __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), ndr2));
                     dp[e >> 1] = pack_bf16(g.x, g.y);
                 }
-                tmem_st16(tmem + lane_off + kColDP + c * 16, dp);
+            };
+            if (h == 0) {
+                // read dP columns 0-63 first: the packed dS of both warpgroups lands in them
+                uint32_t s0[32], s1[32], d0[32], d1[32];
+                tmem_ld32(tmem + lane_off + kColS, s0);
+                tmem_ld32(tmem + lane_off + kColS + 32, s1);
+                tmem_ld32(tmem + lane_off + kColDP, d0);
+                tmem_ld32(tmem + lane_off + kColDP + 32, d1);
+                tmem_wait_ld();
+                reg_fence(s0);
+                reg_fence(s1);
+                reg_fence(d0);
+                reg_fence(d1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_half);
+                uint32_t dp[16];
+                chunk(0, s0, d0, dp);
+                tmem_st16(tmem + lane_off + kColDP, dp);
+                chunk(1, s1, d1, dp);
+                tmem_st16(tmem + lane_off + kColDP + 16, dp);
+            } else {
+#pragma unroll 1
+                for (int c = 2; c < 4; ++c) {
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32(tmem + lane_off + kColS + c * 32, sr);
+                    tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
+                    tmem_wait_ld();
+                    reg_fence(sr);
+                    reg_fence(dr);
+                    uint32_t dp[16];
+                    chunk(c, sr, dr, dp);
+                    if (c == 2) {   // dP columns 32-63 are overwritten below: wait until they were read
+                        ok = wait_abort_warp(bar_half, n & 1, p.err, kSiteBwP, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    tmem_st16(tmem + lane_off + kColDP + c * 16, dp);
+                }
+                if (!ok) break;
             }
             tmem_wait_st();
             tc_fence_before();
@@ -645,8 +683,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) {
             __nv_bfloat16 *dst =
                 static_cast<__nv_bfloat16 *>(p.dQ) + (static_cast<size_t>(bh) * N + (q < N ? q : 0)) * D;
+            // each warpgroup writes half of the dQ columns
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
                 uint32_t a[32];
                 if (nsteps > 0) {
                     tmem_ld32(tmem + lane_off + kColAcc + c * 32, a);
@@ -704,7 +743,7 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int T = (p.N + BT - 1) / BT;
     const dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(T));
-    bwd_dkdv_kernel<D><<<grid, kDkdvThreads, smem, stream>>>(tm, p);
+    bwd_dkdv_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tm, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     bwd_dq_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tm, p);

@@ -158,6 +158,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // the first compute warpgroup has read score columns 0-63, which the second
     // warpgroup's packed P^T / dS^T (query columns 64-127) then overwrite
     const uint32_t bar_half = bars + 8u * 8;
+    // d = 64: P^T and dS^T go to their own TMEM columns [384, 512), so the S^T and dP^T
+    // regions are free once read (bar_sdp_free) and the next step's S^T, dP^T run
+    // during this step's compute; bar_pds_free says dV/dK have read the P^T/dS^T region.
+    constexpr bool kPipe = (D == 64);
+    constexpr uint32_t kColP = 384, kColDS = 448;
+    const uint32_t bar_sdp_free = bars + 8u * 9, bar_pds_free = bars + 8u * 10;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
@@ -183,6 +189,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar_ps, 8);
         mbar_init(bar_done, 1);
         mbar_init(bar_half, 4);
+        mbar_init(bar_sdp_free, 8);
+        mbar_init(bar_pds_free, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -261,7 +269,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, 0, 0);
             constexpr uint32_t idesc_g = idesc_bf16_f32(BT, D, 0, 1);
             bool ok = wait_abort_warp(bar_kv, 0, p.err, kSiteBwKV, abort_flag);
-            for (int n = 0; n < nsteps && ok; ++n) {
+            if constexpr (kPipe) {
+                const uint64_t kd = sdesc_sw128(k_smem, 16, 1024), vd = sdesc_sw128(v_smem, 16, 1024);
+                auto issue_sdp = [&](int n) {   // S^T(n) = K Q_n^T, dP^T(n) = V dO_n^T
+                    const int s = n % C::kStages;
+                    const uint64_t qd = sdesc_sw128(q_stage(s), 16, 1024), od = sdesc_sw128(do_stage(s), 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+                        mma_ss_warp(tmem + kColS, kd + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+                        mma_ss_warp(tmem + kColDP, vd + off, od + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                };
+                if (ok) ok = wait_abort_warp(bar_full(0), 0, p.err, kSiteBwQD, abort_flag);
+                if (ok) {
+                    tc_fence_after();
+                    issue_sdp(0);
+                    mma_commit_warp(bar_st);
+                }
+                for (int n = 0; n < nsteps && ok; ++n) {
+                    const int s = n % C::kStages;
+                    if (n + 1 < nsteps) {
+                        ok = wait_abort_warp(bar_full((n + 1) % C::kStages), ((n + 1) / C::kStages) & 1, p.err,
+                                             kSiteBwQD, abort_flag);
+                        // S^T(n), dP^T(n) read by the compute warpgroups
+                        if (ok) ok = wait_abort_warp(bar_sdp_free, n & 1, p.err, kSiteBwP, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_sdp(n + 1);
+                        mma_commit_warp(bar_st);
+                    }
+                    ok = wait_abort_warp(bar_ps, n & 1, p.err, kSiteBwP, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t odm = sdesc_sw128(do_stage(s), BT * 128, 1024);
+                    const uint64_t qdm = sdesc_sw128(q_stage(s), BT * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ts_warp(tmem + kColAcc, tmem + kColP + kk * 8, odm + ((kk * 2048) >> 4), idesc_g,
+                                    (n > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ts_warp(tmem + kColAcc + D, tmem + kColDS + kk * 8, qdm + ((kk * 2048) >> 4), idesc_g,
+                                    (n > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit_warp(bar_empty(s));
+                    mma_commit_warp(bar_pds_free);
+                }
+            }
+            for (int n = 0; n < nsteps && ok && !kPipe; ++n) {
                 const int s = n % C::kStages;
                 ok = wait_abort_warp(bar_full(s), (n / C::kStages) & 1, p.err, kSiteBwQD, abort_flag);
                 if (!ok) break;
@@ -360,7 +419,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     dp[(e >> 1) + 1] = pack_bf16(g1.x, g1.y);
                 }
             };
-            if (h == 0) {
+            if constexpr (kPipe) {
+#pragma unroll 1
+                for (int c = 2 * h; c < 2 * h + 2; ++c) {
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32(tmem + lane_off + kColS + c * 32, sr);
+                    tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
+                    tmem_wait_ld();
+                    reg_fence(sr);
+                    reg_fence(dr);
+                    if (c == 2 * h + 1) {   // this warp has read its S^T, dP^T columns
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_sdp_free);
+                    }
+                    uint32_t pp[16], dp[16];
+                    chunk(c, sr, dr, pp, dp);
+                    if (c == 2 * h && n > 0) {   // dV/dK of step n-1 have read the P^T/dS^T region
+                        ok = wait_abort_warp(bar_pds_free, (n - 1) & 1, p.err, kSiteBwP, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    tmem_st16(tmem + lane_off + kColP + c * 16, pp);
+                    tmem_st16(tmem + lane_off + kColDS + c * 16, dp);
+                }
+                if (!ok) break;
+            } else if (h == 0) {
                 // read columns 0-63 of S^T and dP^T first: the packed results of both
                 // warpgroups land in them
                 uint32_t s0[32], s1[32], d0[32], d1[32];

@@ -560,6 +560,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto bar_empty = [&](int s) { return bars + 8u * (3 + s); };
     const uint32_t bar_st = bars + 8u * 5, bar_ps = bars + 8u * 6, bar_done = bars + 8u * 7;
     const uint32_t bar_half = bars + 8u * 8;   // dP columns 0-63 read by the first warpgroup
+    // d = 64: dS goes to its own TMEM columns [384, 448), so S and dP are free once read
+    // (bar_sdp_free) and the next key tile's S, dP run during this step's compute;
+    // bar_ds_free says dQ += dS K has read the dS region.
+    constexpr bool kPipe = (D == 64);
+    constexpr uint32_t kColDSq = 384;
+    const uint32_t bar_sdp_free = bars + 8u * 9, bar_ds_free = bars + 8u * 10;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
@@ -586,6 +592,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar_ps, 8);
         mbar_init(bar_done, 1);
         mbar_init(bar_half, 4);
+        mbar_init(bar_sdp_free, 8);
+        mbar_init(bar_ds_free, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -636,7 +644,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t idesc_g = idesc_bf16_f32(BT, D, 0, 1);
             bool ok = wait_abort_warp(bar_qd, 0, p.err, kSiteBwQD, abort_flag);
             const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), od = sdesc_sw128(do_smem, 16, 1024);
-            for (int n = 0; n < nsteps && ok; ++n) {
+            if constexpr (kPipe) {
+                auto issue_sdp = [&](int n) {   // S = Q K_n^T, dP = dO V_n^T
+                    const int s = n % C::kStages;
+                    const uint64_t kd = sdesc_sw128(k_stage(s), 16, 1024), vd = sdesc_sw128(v_stage(s), 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+                        mma_ss_warp(tmem + kColS, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+                        mma_ss_warp(tmem + kColDP, od + off, vd + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                };
+                if (ok) ok = wait_abort_warp(bar_full(0), 0, p.err, kSiteBwKV, abort_flag);
+                if (ok) {
+                    tc_fence_after();
+                    issue_sdp(0);
+                    mma_commit_warp(bar_st);
+                }
+                for (int n = 0; n < nsteps && ok; ++n) {
+                    const int s = n % C::kStages;
+                    if (n + 1 < nsteps) {
+                        ok = wait_abort_warp(bar_full((n + 1) % C::kStages), ((n + 1) / C::kStages) & 1, p.err,
+                                             kSiteBwKV, abort_flag);
+                        if (ok) ok = wait_abort_warp(bar_sdp_free, n & 1, p.err, kSiteBwP, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_sdp(n + 1);
+                        mma_commit_warp(bar_st);
+                    }
+                    ok = wait_abort_warp(bar_ps, n & 1, p.err, kSiteBwP, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t kdm = sdesc_sw128(k_stage(s), BT * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ts_warp(tmem + kColAcc, tmem + kColDSq + kk * 8, kdm + ((kk * 2048) >> 4), idesc_g,
+                                    (n > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit_warp(bar_empty(s));
+                    mma_commit_warp(bar_ds_free);
+                }
+            }
+            for (int n = 0; n < nsteps && ok && !kPipe; ++n) {
                 const int s = n % C::kStages;
                 ok = wait_abort_warp(bar_full(s), (n / C::kStages) & 1, p.err, kSiteBwKV, abort_flag);
                 if (!ok) break;
@@ -713,7 +765,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     dp[e >> 1] = pack_bf16(g.x, g.y);
                 }
             };
-            if (h == 0) {
+            if constexpr (kPipe) {
+#pragma unroll 1
+                for (int c = 2 * h; c < 2 * h + 2; ++c) {
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32(tmem + lane_off + kColS + c * 32, sr);
+                    tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
+                    tmem_wait_ld();
+                    reg_fence(sr);
+                    reg_fence(dr);
+                    if (c == 2 * h + 1) {   // this warp has read its S, dP columns
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_sdp_free);
+                    }
+                    uint32_t dp[16];
+                    chunk(c, sr, dr, dp);
+                    if (c == 2 * h && n > 0) {   // dQ of step n-1 has read the dS region
+                        ok = wait_abort_warp(bar_ds_free, (n - 1) & 1, p.err, kSiteBwP, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    tmem_st16(tmem + lane_off + kColDSq + c * 16, dp);
+                }
+                if (!ok) break;
+            } else if (h == 0) {
                 // read dP columns 0-63 first: the packed dS of both warpgroups lands in them
                 uint32_t s0[32], s1[32], d0[32], d1[32];
                 tmem_ld32(tmem + lane_off + kColS, s0);

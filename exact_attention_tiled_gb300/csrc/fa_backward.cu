@@ -420,30 +420,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             };
             if constexpr (kPipe) {
-#pragma unroll 1
-                for (int c = 2 * h; c < 2 * h + 2; ++c) {
-                    uint32_t sr[32], dr[32];
-                    tmem_ld32(tmem + lane_off + kColS + c * 32, sr);
-                    tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
-                    tmem_wait_ld();
-                    reg_fence(sr);
-                    reg_fence(dr);
-                    if (c == 2 * h + 1) {   // this warp has read its S^T, dP^T columns
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar_sdp_free);
-                    }
-                    uint32_t pp[16], dp[16];
-                    chunk(c, sr, dr, pp, dp);
-                    if (c == 2 * h && n > 0) {   // dV/dK of step n-1 have read the P^T/dS^T region
-                        ok = wait_abort_warp(bar_pds_free, (n - 1) & 1, p.err, kSiteBwP, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
-                    tmem_st16(tmem + lane_off + kColP + c * 16, pp);
-                    tmem_st16(tmem + lane_off + kColDS + c * 16, dp);
+                // read this warpgroup's S^T and dP^T columns at once, then let the MMA
+                // warp start the next step's products while they are computed here
+                const int c0 = 2 * h;
+                uint32_t sa[32], da[32], sb[32], db[32];
+                tmem_ld32(tmem + lane_off + kColS + c0 * 32, sa);
+                tmem_ld32(tmem + lane_off + kColDP + c0 * 32, da);
+                tmem_ld32(tmem + lane_off + kColS + (c0 + 1) * 32, sb);
+                tmem_ld32(tmem + lane_off + kColDP + (c0 + 1) * 32, db);
+                tmem_wait_ld();
+                reg_fence(sa);
+                reg_fence(da);
+                reg_fence(sb);
+                reg_fence(db);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_sdp_free);
+                uint32_t pp[16], dp[16];
+                chunk(c0, sa, da, pp, dp);
+                if (n > 0) {   // dV/dK of step n-1 have read the P^T/dS^T region
+                    ok = wait_abort_warp(bar_pds_free, (n - 1) & 1, p.err, kSiteBwP, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
                 }
-                if (!ok) break;
+                tmem_st16(tmem + lane_off + kColP + c0 * 16, pp);
+                tmem_st16(tmem + lane_off + kColDS + c0 * 16, dp);
+                chunk(c0 + 1, sb, db, pp, dp);
+                tmem_st16(tmem + lane_off + kColP + (c0 + 1) * 16, pp);
+                tmem_st16(tmem + lane_off + kColDS + (c0 + 1) * 16, dp);
             } else if (h == 0) {
                 // read columns 0-63 of S^T and dP^T first: the packed results of both
                 // warpgroups land in them
@@ -766,29 +770,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             };
             if constexpr (kPipe) {
-#pragma unroll 1
-                for (int c = 2 * h; c < 2 * h + 2; ++c) {
-                    uint32_t sr[32], dr[32];
-                    tmem_ld32(tmem + lane_off + kColS + c * 32, sr);
-                    tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
-                    tmem_wait_ld();
-                    reg_fence(sr);
-                    reg_fence(dr);
-                    if (c == 2 * h + 1) {   // this warp has read its S, dP columns
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar_sdp_free);
-                    }
-                    uint32_t dp[16];
-                    chunk(c, sr, dr, dp);
-                    if (c == 2 * h && n > 0) {   // dQ of step n-1 has read the dS region
-                        ok = wait_abort_warp(bar_ds_free, (n - 1) & 1, p.err, kSiteBwP, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
-                    tmem_st16(tmem + lane_off + kColDSq + c * 16, dp);
+                // read this warpgroup's S and dP columns at once, then let the MMA warp
+                // start the next key tile's products while they are computed here
+                const int c0 = 2 * h;
+                uint32_t sa[32], da[32], sb[32], db[32];
+                tmem_ld32(tmem + lane_off + kColS + c0 * 32, sa);
+                tmem_ld32(tmem + lane_off + kColDP + c0 * 32, da);
+                tmem_ld32(tmem + lane_off + kColS + (c0 + 1) * 32, sb);
+                tmem_ld32(tmem + lane_off + kColDP + (c0 + 1) * 32, db);
+                tmem_wait_ld();
+                reg_fence(sa);
+                reg_fence(da);
+                reg_fence(sb);
+                reg_fence(db);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_sdp_free);
+                uint32_t dp[16];
+                chunk(c0, sa, da, dp);
+                if (n > 0) {   // dQ of step n-1 has read the dS region
+                    ok = wait_abort_warp(bar_ds_free, (n - 1) & 1, p.err, kSiteBwP, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
                 }
-                if (!ok) break;
+                tmem_st16(tmem + lane_off + kColDSq + c0 * 16, dp);
+                chunk(c0 + 1, sb, db, dp);
+                tmem_st16(tmem + lane_off + kColDSq + (c0 + 1) * 16, dp);
             } else if (h == 0) {
                 // read dP columns 0-63 first: the packed dS of both warpgroups lands in them
                 uint32_t s0[32], s1[32], d0[32], d1[32];

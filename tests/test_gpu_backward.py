@@ -106,3 +106,16 @@ def test_backward_causal_d128_sampled_heads():
         sl = (slice(0, 1), slice(h, h + 1))
         ref = oracle.sdpa_backward(Q[sl], K[sl], V[sl], dO[sl], causal=True, magnitudes=True)
         _check(f"bwd causal h{h}", {k: v[sl] for k, v in got.items()}, ref)
+
+
+def test_backward_is_deterministic():
+    """Every gradient element is written by one CTA (no atomics): two runs agree bit for bit."""
+    Q, K, V, dO = _inputs(2, 4, 1000, 64, seed=420)
+    dev = torch.device("cuda")
+    Qd, Kd, Vd, dOd = (t.to(dev) for t in (Q, K, V, dO))
+    O, L = fa().fa_forward(Qd, Kd, Vd, causal=True)
+    a = fa().fa_backward(Qd, Kd, Vd, O, dOd, L, causal=True)
+    b = fa().fa_backward(Qd, Kd, Vd, O, dOd, L, causal=True)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)

@@ -42,9 +42,12 @@ namespace fa {
 namespace {
 
 constexpr int BT = 128;              // rows of a query or key tile (MMA M and N)
-// warp 0 producer, warp 1 MMA, warps 2-3 idle, two compute warpgroups: the dK/dV
-// kernel splits each step's query columns 0-63 / 64-127, the dQ kernel its key columns
+// warp 0 producer, warp 1 MMA, warps 2-3 idle, then the compute warpgroups: the dQ
+// kernel's two split each step's key columns 0-63 / 64-127, the dK/dV kernel's four
+// take 32 query columns each
 constexpr int kBwdThreads = 384;
+constexpr int kDkdvGroups = 4;
+constexpr int kDkdvThreads = 128 * (1 + kDkdvGroups);
 constexpr int kProd = 0, kMma = 1, kFirstCompute = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -85,11 +88,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-template <int D>
+template <int D, int Stages = 2>
 struct BwdCfg {
     static constexpr int kColBlocks = D / 64;
     static constexpr int kTileBytes = BT * D * 2;
-    static constexpr int kStages = 2;
+    static constexpr int kStages = Stages;
     // dkdv: K, V, then per stage {Q_i, dO_i}, then per stage {L_i * log2 e, D_i}
     // dq:   Q, dO, then per stage {K_j, V_j}
     static constexpr int kFixedOff = 0;
@@ -103,10 +106,22 @@ struct BwdCfg {
     static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
 };
 
-// TMEM: [0,128) S (then P), [128,256) dP (then dS), [256, 256+D) dV or dQ,
-// [256+D, 256+2D) dK.  P and dS are written as packed bf16 pairs over the
-// first 64 columns of their region: the A operand of the second GEMMs.
+// dQ kernel TMEM: [0,128) S (then P), [128,256) dP (then dS), [256, 256+D) dQ.
+// P and dS are written as packed bf16 pairs over the first 64 columns of their
+// region: the A operand of the second GEMM.
 constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
+
+// dK/dV kernel: a step runs as two half-steps of 64 query columns.  TMEM holds
+// kHalfBufs half-step buffers of 128 columns (S^T half, then dP^T half) and
+// then dV, dK; at d = 64 there is room for three buffers, at d = 128 for two.
+// The Q_i/dO_i ring has one stage more at d = 64 (shared memory allows it), so
+// the deeper lookahead does not wait on its loads.
+template <int D>
+struct DkdvShape {
+    static constexpr int kHalfBufs = D == 64 ? 3 : 2;
+    static constexpr int kStages = D == 64 ? 3 : 2;
+    static constexpr uint32_t kColAccum = 128u * kHalfBufs;   // dV; dK at + D
+};
 
 // ---------------------------------------------------------------------------
 // D_i = sum_c dO_ic O_ic.  D/8 lanes per row, one 16-byte vector each.
@@ -139,9 +154,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *O, co
 // under causal masking: key tile j meets the query tiles i >= j).
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDkdvThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
-    using C = BwdCfg<D>;
+    using C = BwdCfg<D, DkdvShape<D>::kStages>;
+    constexpr int NB = DkdvShape<D>::kHalfBufs;
+    constexpr uint32_t kColGrad = DkdvShape<D>::kColAccum;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -153,17 +170,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t bars = sbase + C::kBarOff;
     const uint32_t bar_kv = bars;
     auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto bar_empty = [&](int s) { return bars + 8u * (3 + s); };
-    const uint32_t bar_st = bars + 8u * 5, bar_ps = bars + 8u * 6, bar_done = bars + 8u * 7;
-    // the first compute warpgroup has read score columns 0-63, which the second
-    // warpgroup's packed P^T / dS^T (query columns 64-127) then overwrite
-    const uint32_t bar_half = bars + 8u * 8;
-    // d = 64: P^T and dS^T go to their own TMEM columns [384, 512), so the S^T and dP^T
-    // regions are free once read (bar_sdp_free) and the next step's S^T, dP^T run
-    // during this step's compute; bar_pds_free says dV/dK have read the P^T/dS^T region.
-    constexpr bool kPipe = (D == 64);
-    constexpr uint32_t kColP = 384, kColDS = 448;
-    const uint32_t bar_sdp_free = bars + 8u * 9, bar_pds_free = bars + 8u * 10;
+    auto bar_empty = [&](int s) { return bars + 8u * (1 + C::kStages + s); };
+    // Half-step u = 2n + hf covers query rows [64 hf, 64 hf + 64) of query tile
+    // i_lo + n and uses TMEM buffer u % NB.  bar_st(b): S^T, dP^T of the buffer's
+    // half-step are in TMEM; bar_ps(b): its two warpgroups have written P^T, dS^T.
+    // A buffer's barriers complete once per use, and the next use is issued only
+    // after the MMA warp saw bar_ps of the previous one, so no phase goes unseen.
+    auto bar_st = [&](int bf) { return bars + 8u * (1 + 2 * C::kStages + bf); };
+    auto bar_ps = [&](int bf) { return bars + 8u * (1 + 2 * C::kStages + NB + bf); };
+    const uint32_t bar_done = bars + 8u * (1 + 2 * C::kStages + 2 * NB);
+    static_assert(1 + 2 * C::kStages + 2 * NB + 1 <= C::kNumBars, "barrier slots");
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
@@ -185,12 +201,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar_full(s), 2);    // TMA bytes + the producer warp's L/D stores
             mbar_init(bar_empty(s), 1);
         }
-        mbar_init(bar_st, 1);
-        mbar_init(bar_ps, 8);
+        for (int bf = 0; bf < NB; ++bf) {
+            mbar_init(bar_st(bf), 1);
+            mbar_init(bar_ps(bf), 8);
+        }
         mbar_init(bar_done, 1);
-        mbar_init(bar_half, 4);
-        mbar_init(bar_sdp_free, 8);
-        mbar_init(bar_pds_free, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -266,96 +281,68 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     } else if (warp == kMma) {
         // ================================================= MMA warp
         if (nsteps > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, 0, 0);
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT / 2, 0, 0);   // M 128 keys, N 64 queries
             constexpr uint32_t idesc_g = idesc_bf16_f32(BT, D, 0, 1);
+            const int nhalf = 2 * nsteps;
             bool ok = wait_abort_warp(bar_kv, 0, p.err, kSiteBwKV, abort_flag);
-            if constexpr (kPipe) {
-                const uint64_t kd = sdesc_sw128(k_smem, 16, 1024), vd = sdesc_sw128(v_smem, 16, 1024);
-                auto issue_sdp = [&](int n) {   // S^T(n) = K Q_n^T, dP^T(n) = V dO_n^T
-                    const int s = n % C::kStages;
-                    const uint64_t qd = sdesc_sw128(q_stage(s), 16, 1024), od = sdesc_sw128(do_stage(s), 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                        mma_ss_warp(tmem + kColS, kd + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                        mma_ss_warp(tmem + kColDP, vd + off, od + off, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-                };
-                if (ok) ok = wait_abort_warp(bar_full(0), 0, p.err, kSiteBwQD, abort_flag);
-                if (ok) {
+            const uint64_t kd = sdesc_sw128(k_smem, 16, 1024), vd = sdesc_sw128(v_smem, 16, 1024);
+            // S^T = K Q_h^T and dP^T = V dO_h^T into buffer u % NB (K-major A and B; the
+            // half's 64 query rows start 8 swizzle atoms into each column block).  The
+            // first half of a step waits for its Q_i, dO_i stage.
+            auto issue_sdp = [&](int u) {
+                const int hf = u & 1, n = u >> 1, s = n % C::kStages;
+                const uint32_t col = 128u * (u % NB);
+                if (hf == 0) {
+                    if (!wait_abort_warp(bar_full(s), (n / C::kStages) & 1, p.err, kSiteBwQD, abort_flag))
+                        return false;
                     tc_fence_after();
-                    issue_sdp(0);
-                    mma_commit_warp(bar_st);
                 }
-                for (int n = 0; n < nsteps && ok; ++n) {
-                    const int s = n % C::kStages;
-                    if (n + 1 < nsteps) {
-                        ok = wait_abort_warp(bar_full((n + 1) % C::kStages), ((n + 1) / C::kStages) & 1, p.err,
-                                             kSiteBwQD, abort_flag);
-                        // S^T(n), dP^T(n) read by the compute warpgroups
-                        if (ok) ok = wait_abort_warp(bar_sdp_free, n & 1, p.err, kSiteBwP, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_sdp(n + 1);
-                        mma_commit_warp(bar_st);
-                    }
-                    ok = wait_abort_warp(bar_ps, n & 1, p.err, kSiteBwP, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t odm = sdesc_sw128(do_stage(s), BT * 128, 1024);
-                    const uint64_t qdm = sdesc_sw128(q_stage(s), BT * 128, 1024);
+                const uint32_t rows = hf * (BT / 2) * 128;
+                const uint64_t qd = sdesc_sw128(q_stage(s) + rows, 16, 1024);
+                const uint64_t od = sdesc_sw128(do_stage(s) + rows, 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)
-                        mma_ts_warp(tmem + kColAcc, tmem + kColP + kk * 8, odm + ((kk * 2048) >> 4), idesc_g,
-                                    (n > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)
-                        mma_ts_warp(tmem + kColAcc + D, tmem + kColDS + kk * 8, qdm + ((kk * 2048) >> 4), idesc_g,
-                                    (n > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit_warp(bar_empty(s));
-                    mma_commit_warp(bar_pds_free);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+                    mma_ss_warp(tmem + col, kd + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
-            }
-            for (int n = 0; n < nsteps && ok && !kPipe; ++n) {
-                const int s = n % C::kStages;
-                ok = wait_abort_warp(bar_full(s), (n / C::kStages) & 1, p.err, kSiteBwQD, abort_flag);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+                    mma_ss_warp(tmem + col + 64, vd + off, od + off, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit_warp(bar_st(u % NB));
+                return true;
+            };
+            // dV += P^T dO_h, dK += dS^T Q_h: A from TMEM (warpgroup 2 hf + w packed its 32
+            // query columns into the first 16 of its own 32), B MN-major (d contiguous)
+            auto issue_grad = [&](int u) {
+                const int hf = u & 1, s = (u >> 1) % C::kStages;
+                const uint32_t col = 128u * (u % NB);
+                const uint64_t odm = sdesc_sw128(do_stage(s), BT * 128, 1024);
+                const uint64_t qdm = sdesc_sw128(q_stage(s), BT * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t acol = col + (kk >> 1) * 32 + (kk & 1) * 8;
+                    const uint32_t boff = ((hf * 4 + kk) * 2048) >> 4;   // 16 query rows per step
+                    mma_ts_warp(tmem + kColGrad, tmem + acol, odm + boff, idesc_g, (u > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t acol = col + 64 + (kk >> 1) * 32 + (kk & 1) * 8;
+                    const uint32_t boff = ((hf * 4 + kk) * 2048) >> 4;
+                    mma_ts_warp(tmem + kColGrad + D, tmem + acol, qdm + boff, idesc_g, (u > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
+            for (int u = 0; u < NB && u < nhalf && ok; ++u) ok = issue_sdp(u);
+            // The tensor core runs one thread's MMAs in issue order: S^T/dP^T of half-step
+            // u + NB overwrite the buffer that dV/dK of half-step u read just before.
+            for (int u = 0; u < nhalf && ok; ++u) {
+                ok = wait_abort_warp(bar_ps(u % NB), (u / NB) & 1, p.err, kSiteBwP, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                {   // S^T = K Q_i^T and dP^T = V dO_i^T (K-major A and B)
-                    const uint64_t kd = sdesc_sw128(k_smem, 16, 1024), vd = sdesc_sw128(v_smem, 16, 1024);
-                    const uint64_t qd = sdesc_sw128(q_stage(s), 16, 1024), od = sdesc_sw128(do_stage(s), 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                        mma_ss_warp(tmem + kColS, kd + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                        mma_ss_warp(tmem + kColDP, vd + off, od + off, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-                }
-                mma_commit_warp(bar_st);
-                ok = wait_abort_warp(bar_ps, n & 1, p.err, kSiteBwP, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                {   // dV += P^T dO_i, dK += dS^T Q_i (A from TMEM, B MN-major: d contiguous)
-                    const uint64_t odm = sdesc_sw128(do_stage(s), BT * 128, 1024);
-                    const uint64_t qdm = sdesc_sw128(q_stage(s), BT * 128, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)
-                        mma_ts_warp(tmem + kColAcc, tmem + kColS + kk * 8, odm + ((kk * 2048) >> 4), idesc_g,
-                                    (n > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)
-                        mma_ts_warp(tmem + kColAcc + D, tmem + kColDP + kk * 8, qdm + ((kk * 2048) >> 4), idesc_g,
-                                    (n > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit_warp(bar_empty(s));   // Q_i, dO_i read: the stage is free
+                issue_grad(u);
+                if (u & 1) mma_commit_warp(bar_empty((u >> 1) % C::kStages));   // Q_i, dO_i read
+                if (u + NB < nhalf) ok = issue_sdp(u + NB);
             }
             // every MMA has completed before the gradients are read and TMEM is freed
             mma_commit_warp(bar_done);
@@ -364,7 +351,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp >= kFirstCompute) {
         // ================================================= compute warpgroups
-        // warpgroup h handles query columns [64h, 64h + 64) of every step, one
+        // warpgroup h handles query columns [32h, 32h + 32) of every step, one
         // thread per key row (TMEM lane)
         const int h = (warp - kFirstCompute) >> 2;
         const int quarter = warp & 3;
@@ -375,10 +362,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float sl2 = p.scale_log2;
         const float2 sl22 = make_float2(sl2, sl2);
         bool ok = true;
+        const int hf = h >> 1;   // the half of every step this warpgroup serves
+        const int w = h & 1;     // its 32 columns within the half
         for (int n = 0; n < nsteps && ok; ++n) {
             const int s = n % C::kStages;
             const int q0 = (i_lo + n) * BT;
-            ok = wait_abort_warp(bar_st, n & 1, p.err, kSiteBwS, abort_flag);
+            const int u = 2 * n + hf;
+            const uint32_t col = 128u * (u % NB) + 32u * w;
+            ok = wait_abort_warp(bar_st(u % NB), (u / NB) & 1, p.err, kSiteBwS, abort_flag);
             // the producer warp's L_i / D_i stores are published by the stage's
             // full barrier (already complete here: the MMAs behind bar_st waited on it)
             if (ok) ok = wait_abort_warp(bar_full(s), (n / C::kStages) & 1, p.err, kSiteBwQD, abort_flag);
@@ -419,83 +410,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     dp[(e >> 1) + 1] = pack_bf16(g1.x, g1.y);
                 }
             };
-            if constexpr (kPipe) {
-                // read this warpgroup's S^T and dP^T columns at once, then let the MMA
-                // warp start the next step's products while they are computed here
-                const int c0 = 2 * h;
-                uint32_t sa[32], da[32], sb[32], db[32];
-                tmem_ld32(tmem + lane_off + kColS + c0 * 32, sa);
-                tmem_ld32(tmem + lane_off + kColDP + c0 * 32, da);
-                tmem_ld32(tmem + lane_off + kColS + (c0 + 1) * 32, sb);
-                tmem_ld32(tmem + lane_off + kColDP + (c0 + 1) * 32, db);
-                tmem_wait_ld();
-                reg_fence(sa);
-                reg_fence(da);
-                reg_fence(sb);
-                reg_fence(db);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_sdp_free);
-                uint32_t pp[16], dp[16];
-                chunk(c0, sa, da, pp, dp);
-                if (n > 0) {   // dV/dK of step n-1 have read the P^T/dS^T region
-                    ok = wait_abort_warp(bar_pds_free, (n - 1) & 1, p.err, kSiteBwP, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                tmem_st16(tmem + lane_off + kColP + c0 * 16, pp);
-                tmem_st16(tmem + lane_off + kColDS + c0 * 16, dp);
-                chunk(c0 + 1, sb, db, pp, dp);
-                tmem_st16(tmem + lane_off + kColP + (c0 + 1) * 16, pp);
-                tmem_st16(tmem + lane_off + kColDS + (c0 + 1) * 16, dp);
-            } else if (h == 0) {
-                // read columns 0-63 of S^T and dP^T first: the packed results of both
-                // warpgroups land in them
-                uint32_t s0[32], s1[32], d0[32], d1[32];
-                tmem_ld32(tmem + lane_off + kColS, s0);
-                tmem_ld32(tmem + lane_off + kColS + 32, s1);
-                tmem_ld32(tmem + lane_off + kColDP, d0);
-                tmem_ld32(tmem + lane_off + kColDP + 32, d1);
-                tmem_wait_ld();
-                reg_fence(s0);
-                reg_fence(s1);
-                reg_fence(d0);
-                reg_fence(d1);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_half);
-                uint32_t pp[16], dp[16];
-                chunk(0, s0, d0, pp, dp);
-                tmem_st16(tmem + lane_off + kColS, pp);
-                tmem_st16(tmem + lane_off + kColDP, dp);
-                chunk(1, s1, d1, pp, dp);
-                tmem_st16(tmem + lane_off + kColS + 16, pp);
-                tmem_st16(tmem + lane_off + kColDP + 16, dp);
-            } else {
-#pragma unroll 1
-                for (int c = 2; c < 4; ++c) {
-                    uint32_t sr[32], dr[32];
-                    tmem_ld32(tmem + lane_off + kColS + c * 32, sr);
-                    tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
-                    tmem_wait_ld();
-                    reg_fence(sr);
-                    reg_fence(dr);
-                    uint32_t pp[16], dp[16];
-                    chunk(c, sr, dr, pp, dp);
-                    if (c == 2) {   // columns 32-63 are overwritten below: wait until they were read
-                        ok = wait_abort_warp(bar_half, n & 1, p.err, kSiteBwP, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
-                    tmem_st16(tmem + lane_off + kColS + c * 16, pp);
-                    tmem_st16(tmem + lane_off + kColDP + c * 16, dp);
-                }
-                if (!ok) break;
-            }
+            // this warpgroup's S^T and dP^T columns; P^T and dS^T are packed over the
+            // first 16 of them
+            uint32_t sr[32], dr[32];
+            tmem_ld32(tmem + lane_off + col, sr);
+            tmem_ld32(tmem + lane_off + col + 64, dr);
+            tmem_wait_ld();
+            reg_fence(sr);
+            reg_fence(dr);
+            uint32_t pp[16], dp[16];
+            chunk(h, sr, dr, pp, dp);
+            tmem_st16(tmem + lane_off + col, pp);
+            tmem_st16(tmem + lane_off + col + 64, dp);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_ps);
+            if (lane == 0) mbar_arrive(bar_ps(u % NB));
         }
         // ---- epilogue: dV and dK (x scale) to bf16; keys with no step get zeros
         if (ok && nsteps > 0) {
@@ -507,14 +437,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) {
             const size_t row = (static_cast<size_t>(bh) * N + (key < N ? key : 0)) * D;
             {
-                const int which = h;   // warpgroup 0 writes dV, warpgroup 1 dK
+                // warpgroups 0, 1 write the two column halves of dV, warpgroups 2, 3 of dK
+                const int which = h >> 1;
                 __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(which ? p.dK : p.dV) + row;
                 const float mul = which ? p.scale : 1.f;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = (h & 1) * (D / 64); c < (h & 1) * (D / 64) + D / 64; ++c) {
                     uint32_t a[32];
                     if (nsteps > 0) {
-                        tmem_ld32(tmem + lane_off + kColAcc + which * D + c * 32, a);
+                        tmem_ld32(tmem + lane_off + kColGrad + which * D + c * 32, a);
                         tmem_wait_ld();
                         reg_fence(a);
                     } else {
@@ -903,14 +834,14 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     if (!make_map(&tm.q, p.Q, BH, p.N, D) || !make_map(&tm.k, p.K, BH, p.N, D) ||
         !make_map(&tm.v, p.V, BH, p.N, D) || !make_map(&tm.dO, p.dO, BH, p.N, D))
         return cudaErrorInvalidValue;
-    const int smem = BwdCfg<D>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem_kv = BwdCfg<D, DkdvShape<D>::kStages>::kSmemBytes, smem = BwdCfg<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int T = (p.N + BT - 1) / BT;
     const dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(T));
-    bwd_dkdv_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tm, p);
+    bwd_dkdv_kernel<D><<<grid, kDkdvThreads, smem_kv, stream>>>(tm, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     bwd_dq_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tm, p);

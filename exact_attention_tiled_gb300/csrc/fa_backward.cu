@@ -13,21 +13,23 @@
 // Three kernels, no N x N matrix in global memory:
 //   * bwd_pre_kernel: D = rowsum(dO o O) in fp32 (bandwidth bound).
 //   * bwd_dkdv_kernel: one CTA per 128-key tile j of one (b, h).  K_j and V_j
-//     stay in shared memory; the query tiles i stream through a 2-stage ring
-//     together with their dO_i, L_i and D_i.  Per step the tensor core forms
-//     S^T = K_j Q_i^T and dP^T = V_j dO_i^T in TMEM (keys on the 128 TMEM
-//     lanes, queries on the columns); the compute warpgroup turns them into
-//     P^T and dS^T (bf16, written back over the first half of each), and the
-//     tensor core accumulates dV += P^T dO_i and dK += dS^T Q_i in TMEM with
-//     A read straight from TMEM.  dV, dK leave once, at the end.
-//   * bwd_dq_kernel: one CTA per 128-query tile i: S = Q_i K_j^T and
-//     dP = dO_i V_j^T per key tile, dS in the compute warpgroup, and
-//     dQ += dS K_j in TMEM.  Computing dQ in its own pass (recomputing S and
-//     dP) keeps every gradient element written by exactly one CTA: no atomics,
-//     and the result does not depend on scheduling.
-// Warp roles in both main kernels (256 threads): warp 0 lane 0 issues the
+//     stay in shared memory; the query tiles i stream through a ring together
+//     with their dO_i, L_i and D_i.  Per half of a query tile (64 queries) the
+//     tensor core forms S^T = K_j Q_i^T and dP^T = V_j dO_i^T in TMEM (keys on
+//     the 128 TMEM lanes, queries on the columns); two compute warpgroups turn
+//     them into P^T and dS^T (bf16, packed over the first half of each
+//     warpgroup's columns), and the tensor core accumulates dV += P^T dO_i and
+//     dK += dS^T Q_i in TMEM with A read straight from TMEM.  Each half has its
+//     own TMEM buffer, so one half's exponentials overlap the other half's
+//     products.  dV, dK leave once, at the end.
+//   * bwd_dq_kernel: one CTA per 128-query tile i, the same half-step scheme
+//     over key tiles: S = Q_i K_j^T and dP = dO_i V_j^T, dS in the compute
+//     warpgroups, and dQ += dS K_j in TMEM.  Computing dQ in its own pass
+//     (recomputing S and dP) keeps every gradient element written by exactly
+//     one CTA: no atomics, and the result does not depend on scheduling.
+// Warp roles in both main kernels (640 threads): warp 0 lane 0 issues the
 // TMA copies, warp 1 is the MMA warp (converged, one elected lane issues),
-// warps 4-7 are the compute warpgroup, one thread per TMEM lane (tile row).
+// warps 4-19 are four compute warpgroups, one thread per TMEM lane (tile row).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -42,12 +44,11 @@ namespace fa {
 namespace {
 
 constexpr int BT = 128;              // rows of a query or key tile (MMA M and N)
-// warp 0 producer, warp 1 MMA, warps 2-3 idle, then the compute warpgroups: the dQ
-// kernel's two split each step's key columns 0-63 / 64-127, the dK/dV kernel's four
-// take 32 query columns each
-constexpr int kBwdThreads = 384;
-constexpr int kDkdvGroups = 4;
-constexpr int kDkdvThreads = 128 * (1 + kDkdvGroups);
+// warp 0 producer, warp 1 MMA, warps 2-3 idle, then four compute warpgroups that
+// take 32 columns each of every step (query columns in the dK/dV kernel, key
+// columns in the dQ kernel); warpgroups 2 hf and 2 hf + 1 serve half-step hf
+constexpr int kComputeGroups = 4;
+constexpr int kBwdThreads = 128 * (1 + kComputeGroups);
 constexpr int kProd = 0, kMma = 1, kFirstCompute = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -106,18 +107,14 @@ struct BwdCfg {
     static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
 };
 
-// dQ kernel TMEM: [0,128) S (then P), [128,256) dP (then dS), [256, 256+D) dQ.
-// P and dS are written as packed bf16 pairs over the first 64 columns of their
-// region: the A operand of the second GEMM.
-constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
-
-// dK/dV kernel: a step runs as two half-steps of 64 query columns.  TMEM holds
-// kHalfBufs half-step buffers of 128 columns (S^T half, then dP^T half) and
-// then dV, dK; at d = 64 there is room for three buffers, at d = 128 for two.
-// The Q_i/dO_i ring has one stage more at d = 64 (shared memory allows it), so
-// the deeper lookahead does not wait on its loads.
+// Both main kernels run a step (one 128-row tile of the streamed operand) as two
+// half-steps of 64 columns.  TMEM holds kHalfBufs half-step buffers of 128
+// columns (S half, then dP half) and then the accumulators; at d = 64 there is
+// room for three buffers, at d = 128 for two.  The streamed ring has one stage
+// more at d = 64 (shared memory allows it), so the deeper lookahead does not
+// wait on its loads.
 template <int D>
-struct DkdvShape {
+struct HalfStepShape {
     static constexpr int kHalfBufs = D == 64 ? 3 : 2;
     static constexpr int kStages = D == 64 ? 3 : 2;
     static constexpr uint32_t kColAccum = 128u * kHalfBufs;   // dV; dK at + D
@@ -154,11 +151,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *O, co
 // under causal masking: key tile j meets the query tiles i >= j).
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kDkdvThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
-    using C = BwdCfg<D, DkdvShape<D>::kStages>;
-    constexpr int NB = DkdvShape<D>::kHalfBufs;
-    constexpr uint32_t kColGrad = DkdvShape<D>::kColAccum;
+    using C = BwdCfg<D, HalfStepShape<D>::kStages>;
+    constexpr int NB = HalfStepShape<D>::kHalfBufs;
+    constexpr uint32_t kColGrad = HalfStepShape<D>::kColAccum;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -481,7 +478,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
-    using C = BwdCfg<D>;
+    using C = BwdCfg<D, HalfStepShape<D>::kStages>;
+    constexpr int NB = HalfStepShape<D>::kHalfBufs;
+    constexpr uint32_t kColGrad = HalfStepShape<D>::kColAccum;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -492,15 +491,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t bars = sbase + C::kBarOff;
     const uint32_t bar_qd = bars;
     auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto bar_empty = [&](int s) { return bars + 8u * (3 + s); };
-    const uint32_t bar_st = bars + 8u * 5, bar_ps = bars + 8u * 6, bar_done = bars + 8u * 7;
-    const uint32_t bar_half = bars + 8u * 8;   // dP columns 0-63 read by the first warpgroup
-    // d = 64: dS goes to its own TMEM columns [384, 448), so S and dP are free once read
-    // (bar_sdp_free) and the next key tile's S, dP run during this step's compute;
-    // bar_ds_free says dQ += dS K has read the dS region.
-    constexpr bool kPipe = (D == 64);
-    constexpr uint32_t kColDSq = 384;
-    const uint32_t bar_sdp_free = bars + 8u * 9, bar_ds_free = bars + 8u * 10;
+    auto bar_empty = [&](int s) { return bars + 8u * (1 + C::kStages + s); };
+    // half-step u = 2n + hf: key rows [64 hf, 64 hf + 64) of key tile n, TMEM buffer
+    // u % NB; the barriers follow the dK/dV kernel's
+    auto bar_st = [&](int bf) { return bars + 8u * (1 + 2 * C::kStages + bf); };
+    auto bar_ps = [&](int bf) { return bars + 8u * (1 + 2 * C::kStages + NB + bf); };
+    const uint32_t bar_done = bars + 8u * (1 + 2 * C::kStages + 2 * NB);
+    static_assert(1 + 2 * C::kStages + 2 * NB + 1 <= C::kNumBars, "barrier slots");
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
@@ -523,12 +520,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar_full(s), 1);
             mbar_init(bar_empty(s), 1);
         }
-        mbar_init(bar_st, 1);
-        mbar_init(bar_ps, 8);
+        for (int bf = 0; bf < NB; ++bf) {
+            mbar_init(bar_st(bf), 1);
+            mbar_init(bar_ps(bf), 8);
+        }
         mbar_init(bar_done, 1);
-        mbar_init(bar_half, 4);
-        mbar_init(bar_sdp_free, 8);
-        mbar_init(bar_ds_free, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -575,92 +571,70 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp == kMma) {
         if (nsteps > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, 0, 0);
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT / 2, 0, 0);   // M 128 queries, N 64 keys
             constexpr uint32_t idesc_g = idesc_bf16_f32(BT, D, 0, 1);
+            const int nhalf = 2 * nsteps;
             bool ok = wait_abort_warp(bar_qd, 0, p.err, kSiteBwQD, abort_flag);
             const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), od = sdesc_sw128(do_smem, 16, 1024);
-            if constexpr (kPipe) {
-                auto issue_sdp = [&](int n) {   // S = Q K_n^T, dP = dO V_n^T
-                    const int s = n % C::kStages;
-                    const uint64_t kd = sdesc_sw128(k_stage(s), 16, 1024), vd = sdesc_sw128(v_stage(s), 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                        mma_ss_warp(tmem + kColS, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                        mma_ss_warp(tmem + kColDP, od + off, vd + off, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-                };
-                if (ok) ok = wait_abort_warp(bar_full(0), 0, p.err, kSiteBwKV, abort_flag);
-                if (ok) {
+            // S = Q K_h^T, dP = dO V_h^T into buffer u % NB; the first half of a key tile
+            // waits for its K_j, V_j stage
+            auto issue_sdp = [&](int u) {
+                const int hf = u & 1, n = u >> 1, s = n % C::kStages;
+                const uint32_t col = 128u * (u % NB);
+                if (hf == 0) {
+                    if (!wait_abort_warp(bar_full(s), (n / C::kStages) & 1, p.err, kSiteBwKV, abort_flag))
+                        return false;
                     tc_fence_after();
-                    issue_sdp(0);
-                    mma_commit_warp(bar_st);
                 }
-                for (int n = 0; n < nsteps && ok; ++n) {
-                    const int s = n % C::kStages;
-                    if (n + 1 < nsteps) {
-                        ok = wait_abort_warp(bar_full((n + 1) % C::kStages), ((n + 1) / C::kStages) & 1, p.err,
-                                             kSiteBwKV, abort_flag);
-                        if (ok) ok = wait_abort_warp(bar_sdp_free, n & 1, p.err, kSiteBwP, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_sdp(n + 1);
-                        mma_commit_warp(bar_st);
-                    }
-                    ok = wait_abort_warp(bar_ps, n & 1, p.err, kSiteBwP, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t kdm = sdesc_sw128(k_stage(s), BT * 128, 1024);
+                const uint32_t rows = hf * (BT / 2) * 128;
+                const uint64_t kd = sdesc_sw128(k_stage(s) + rows, 16, 1024);
+                const uint64_t vd = sdesc_sw128(v_stage(s) + rows, 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)
-                        mma_ts_warp(tmem + kColAcc, tmem + kColDSq + kk * 8, kdm + ((kk * 2048) >> 4), idesc_g,
-                                    (n > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit_warp(bar_empty(s));
-                    mma_commit_warp(bar_ds_free);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+                    mma_ss_warp(tmem + col, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
-            }
-            for (int n = 0; n < nsteps && ok && !kPipe; ++n) {
-                const int s = n % C::kStages;
-                ok = wait_abort_warp(bar_full(s), (n / C::kStages) & 1, p.err, kSiteBwKV, abort_flag);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
+                    mma_ss_warp(tmem + col + 64, od + off, vd + off, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit_warp(bar_st(u % NB));
+                return true;
+            };
+            // dQ += dS K_h: A = dS from TMEM (packed over the first 16 of each warpgroup's
+            // 32 dP columns), B = K_h MN-major
+            auto issue_grad = [&](int u) {
+                const int hf = u & 1, s = (u >> 1) % C::kStages;
+                const uint32_t col = 128u * (u % NB) + 64;
+                const uint64_t kdm = sdesc_sw128(k_stage(s), BT * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t acol = col + (kk >> 1) * 32 + (kk & 1) * 8;
+                    const uint32_t boff = ((hf * 4 + kk) * 2048) >> 4;   // 16 key rows per step
+                    mma_ts_warp(tmem + kColGrad, tmem + acol, kdm + boff, idesc_g, (u > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
+            for (int u = 0; u < NB && u < nhalf && ok; ++u) ok = issue_sdp(u);
+            // S/dP of half-step u + NB overwrite the buffer that dQ of half-step u read
+            // just before (the tensor core runs one thread's MMAs in issue order)
+            for (int u = 0; u < nhalf && ok; ++u) {
+                ok = wait_abort_warp(bar_ps(u % NB), (u / NB) & 1, p.err, kSiteBwP, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                {   // S = Q K_j^T, dP = dO V_j^T
-                    const uint64_t kd = sdesc_sw128(k_stage(s), 16, 1024), vd = sdesc_sw128(v_stage(s), 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                        mma_ss_warp(tmem + kColS, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                        mma_ss_warp(tmem + kColDP, od + off, vd + off, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-                }
-                mma_commit_warp(bar_st);
-                ok = wait_abort_warp(bar_ps, n & 1, p.err, kSiteBwP, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                {   // dQ += dS K_j (A = dS from TMEM, B = K_j MN-major)
-                    const uint64_t kdm = sdesc_sw128(k_stage(s), BT * 128, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)
-                        mma_ts_warp(tmem + kColAcc, tmem + kColDP + kk * 8, kdm + ((kk * 2048) >> 4), idesc_g,
-                                    (n > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit_warp(bar_empty(s));
+                issue_grad(u);
+                if (u & 1) mma_commit_warp(bar_empty((u >> 1) % C::kStages));   // K_j, V_j read
+                if (u + NB < nhalf) ok = issue_sdp(u + NB);
             }
             mma_commit_warp(bar_done);
             mbar_wait(bar_done, 0, p.err, kSiteBwDone);
             __syncwarp();
         }
     } else if (warp >= kFirstCompute) {
-        // warpgroup h handles key columns [64h, 64h + 64) of every step, one thread per query row
+        // warpgroup h handles key columns [32h, 32h + 32) of every key tile (half-step
+        // h / 2, columns 32 (h & 1) of its buffer), one thread per query row
         const int h = (warp - kFirstCompute) >> 2;
+        const int hf = h >> 1, w = h & 1;
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const int q = q0 + r;
@@ -675,102 +649,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float2 ndr2 = make_float2(-drow, -drow);
         bool ok = true;
         for (int n = 0; n < nsteps && ok; ++n) {
-            ok = wait_abort_warp(bar_st, n & 1, p.err, kSiteBwS, abort_flag);
+            const int u = 2 * n + hf;
+            const uint32_t col = 128u * (u % NB) + 32u * w;
+            ok = wait_abort_warp(bar_st(u % NB), (u / NB) & 1, p.err, kSiteBwS, abort_flag);
             if (!ok) break;
             tc_fence_after();
             __syncwarp();
-            const int kb = n * BT;
+            const int kb = n * BT + h * 32;   // first key of this warpgroup's columns
             // masking only where the key tile touches key_len, the diagonal or the row tail
-            const bool need_mask = kb + BT > klen || q0 + BT > N || (p.causal && kb + BT - 1 > q0);
-            // dS of the 32-key chunk c (packed bf16 pairs) from its S and dP values
-            auto chunk = [&](int c, uint32_t (&sr)[32], const uint32_t (&dr)[32], uint32_t (&dp)[16]) {
-                if (need_mask) {
+            const bool need_mask = n * BT + BT > klen || q0 + BT > N || (p.causal && n * BT + BT - 1 > q0);
+            uint32_t sr[32], dr[32];
+            tmem_ld32(tmem + lane_off + col, sr);
+            tmem_ld32(tmem + lane_off + col + 64, dr);
+            tmem_wait_ld();
+            reg_fence(sr);
+            reg_fence(dr);
+            if (need_mask) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int key = kb + c * 32 + e;
-                        if (!(q < N && key < klen && (!p.causal || key <= q))) sr[e] = __float_as_uint(-INFINITY);
-                    }
+                for (int e = 0; e < 32; ++e) {
+                    const int key = kb + e;
+                    if (!(q < N && key < klen && (!p.causal || key <= q))) sr[e] = __float_as_uint(-INFINITY);
                 }
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl22, nl2);
-                    const float2 pr = make_float2(ex2(x.x), ex2(x.y));
-                    const float2 g =
-                        __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), ndr2));
-                    dp[e >> 1] = pack_bf16(g.x, g.y);
-                }
-            };
-            if constexpr (kPipe) {
-                // read this warpgroup's S and dP columns at once, then let the MMA warp
-                // start the next key tile's products while they are computed here
-                const int c0 = 2 * h;
-                uint32_t sa[32], da[32], sb[32], db[32];
-                tmem_ld32(tmem + lane_off + kColS + c0 * 32, sa);
-                tmem_ld32(tmem + lane_off + kColDP + c0 * 32, da);
-                tmem_ld32(tmem + lane_off + kColS + (c0 + 1) * 32, sb);
-                tmem_ld32(tmem + lane_off + kColDP + (c0 + 1) * 32, db);
-                tmem_wait_ld();
-                reg_fence(sa);
-                reg_fence(da);
-                reg_fence(sb);
-                reg_fence(db);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_sdp_free);
-                uint32_t dp[16];
-                chunk(c0, sa, da, dp);
-                if (n > 0) {   // dQ of step n-1 has read the dS region
-                    ok = wait_abort_warp(bar_ds_free, (n - 1) & 1, p.err, kSiteBwP, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                tmem_st16(tmem + lane_off + kColDSq + c0 * 16, dp);
-                chunk(c0 + 1, sb, db, dp);
-                tmem_st16(tmem + lane_off + kColDSq + (c0 + 1) * 16, dp);
-            } else if (h == 0) {
-                // read dP columns 0-63 first: the packed dS of both warpgroups lands in them
-                uint32_t s0[32], s1[32], d0[32], d1[32];
-                tmem_ld32(tmem + lane_off + kColS, s0);
-                tmem_ld32(tmem + lane_off + kColS + 32, s1);
-                tmem_ld32(tmem + lane_off + kColDP, d0);
-                tmem_ld32(tmem + lane_off + kColDP + 32, d1);
-                tmem_wait_ld();
-                reg_fence(s0);
-                reg_fence(s1);
-                reg_fence(d0);
-                reg_fence(d1);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_half);
-                uint32_t dp[16];
-                chunk(0, s0, d0, dp);
-                tmem_st16(tmem + lane_off + kColDP, dp);
-                chunk(1, s1, d1, dp);
-                tmem_st16(tmem + lane_off + kColDP + 16, dp);
-            } else {
-#pragma unroll 1
-                for (int c = 2; c < 4; ++c) {
-                    uint32_t sr[32], dr[32];
-                    tmem_ld32(tmem + lane_off + kColS + c * 32, sr);
-                    tmem_ld32(tmem + lane_off + kColDP + c * 32, dr);
-                    tmem_wait_ld();
-                    reg_fence(sr);
-                    reg_fence(dr);
-                    uint32_t dp[16];
-                    chunk(c, sr, dr, dp);
-                    if (c == 2) {   // dP columns 32-63 are overwritten below: wait until they were read
-                        ok = wait_abort_warp(bar_half, n & 1, p.err, kSiteBwP, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
-                    tmem_st16(tmem + lane_off + kColDP + c * 16, dp);
-                }
-                if (!ok) break;
             }
+            // dS = P (dP - D), P = 2^(S scale log2 e - L log2 e), packed over the first 16
+            // of this warpgroup's dP columns
+            uint32_t dp[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl22, nl2);
+                const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+                const float2 g =
+                    __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), ndr2));
+                dp[e >> 1] = pack_bf16(g.x, g.y);
+            }
+            tmem_st16(tmem + lane_off + col + 64, dp);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_ps);
+            if (lane == 0) mbar_arrive(bar_ps(u % NB));
         }
         if (ok && nsteps > 0) {
             ok = wait_abort_warp(bar_done, 0, p.err, kSiteBwDone, abort_flag);
@@ -781,12 +697,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) {
             __nv_bfloat16 *dst =
                 static_cast<__nv_bfloat16 *>(p.dQ) + (static_cast<size_t>(bh) * N + (q < N ? q : 0)) * D;
-            // each warpgroup writes half of the dQ columns
+            // warpgroup h writes dQ columns [32c, 32c + 32) for c = h, h + 4, ...
 #pragma unroll 1
-            for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
+            for (int c = h; c < D / 32; c += kComputeGroups) {
                 uint32_t a[32];
                 if (nsteps > 0) {
-                    tmem_ld32(tmem + lane_off + kColAcc + c * 32, a);
+                    tmem_ld32(tmem + lane_off + kColGrad + c * 32, a);
                     tmem_wait_ld();
                     reg_fence(a);
                 } else {
@@ -834,14 +750,14 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     if (!make_map(&tm.q, p.Q, BH, p.N, D) || !make_map(&tm.k, p.K, BH, p.N, D) ||
         !make_map(&tm.v, p.V, BH, p.N, D) || !make_map(&tm.dO, p.dO, BH, p.N, D))
         return cudaErrorInvalidValue;
-    const int smem_kv = BwdCfg<D, DkdvShape<D>::kStages>::kSmemBytes, smem = BwdCfg<D>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv);
+    const int smem = BwdCfg<D, HalfStepShape<D>::kStages>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int T = (p.N + BT - 1) / BT;
     const dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(T));
-    bwd_dkdv_kernel<D><<<grid, kDkdvThreads, smem_kv, stream>>>(tm, p);
+    bwd_dkdv_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tm, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     bwd_dq_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tm, p);

@@ -481,6 +481,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     using C = BwdCfg<D, HalfStepShape<D>::kStages>;
     constexpr int NB = HalfStepShape<D>::kHalfBufs;
     constexpr uint32_t kColGrad = HalfStepShape<D>::kColAccum;
+    // Q_i and dO_i stay in TMEM as packed bf16 rows (one query per lane): the A
+    // operands of S = Q K^T and dP = dO V^T, so those products read only K and V
+    // from shared memory
+    constexpr uint32_t kColQ = kColGrad + D, kColDO = kColQ + D / 2;
+    static_assert(kColDO + D / 2 <= 512, "TMEM columns");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -497,7 +502,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto bar_st = [&](int bf) { return bars + 8u * (1 + 2 * C::kStages + bf); };
     auto bar_ps = [&](int bf) { return bars + 8u * (1 + 2 * C::kStages + NB + bf); };
     const uint32_t bar_done = bars + 8u * (1 + 2 * C::kStages + 2 * NB);
-    static_assert(1 + 2 * C::kStages + 2 * NB + 1 <= C::kNumBars, "barrier slots");
+    const uint32_t bar_qtm = bars + 8u * (2 + 2 * C::kStages + 2 * NB);   // Q_i, dO_i are in TMEM
+    static_assert(2 + 2 * C::kStages + 2 * NB + 1 <= C::kNumBars, "barrier slots");
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
@@ -525,6 +531,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar_ps(bf), 8);
         }
         mbar_init(bar_done, 1);
+        mbar_init(bar_qtm, 8);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -574,10 +581,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT / 2, 0, 0);   // M 128 queries, N 64 keys
             constexpr uint32_t idesc_g = idesc_bf16_f32(BT, D, 0, 1);
             const int nhalf = 2 * nsteps;
-            bool ok = wait_abort_warp(bar_qd, 0, p.err, kSiteBwQD, abort_flag);
-            const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), od = sdesc_sw128(do_smem, 16, 1024);
-            // S = Q K_h^T, dP = dO V_h^T into buffer u % NB; the first half of a key tile
-            // waits for its K_j, V_j stage
+            bool ok = wait_abort_warp(bar_qtm, 0, p.err, kSiteBwQD, abort_flag);
+            // S = Q K_h^T, dP = dO V_h^T into buffer u % NB, A = Q or dO from TMEM; the
+            // first half of a key tile waits for its K_j, V_j stage
             auto issue_sdp = [&](int u) {
                 const int hf = u & 1, n = u >> 1, s = n % C::kStages;
                 const uint32_t col = 128u * (u % NB);
@@ -592,12 +598,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                    mma_ss_warp(tmem + col, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+                    mma_ts_warp(tmem + col, tmem + kColQ + kk * 8, kd + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                    mma_ss_warp(tmem + col + 64, od + off, vd + off, idesc_s, kk > 0 ? 1u : 0u);
+                    mma_ts_warp(tmem + col + 64, tmem + kColDO + kk * 8, vd + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 mma_commit_warp(bar_st(u % NB));
                 return true;
@@ -648,6 +654,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float2 sl22 = make_float2(sl2, sl2), nl2 = make_float2(-lrow, -lrow);
         const float2 ndr2 = make_float2(-drow, -drow);
         bool ok = true;
+        if (h < 2 && nsteps > 0) {
+            // warpgroup 0 copies this thread's row of Q_i, warpgroup 1 its row of dO_i,
+            // from the swizzled shared tile (16-byte chunk c of row r sits at c ^ (r & 7))
+            // into TMEM columns as packed bf16 pairs
+            ok = wait_abort_warp(bar_qd, 0, p.err, kSiteBwQD, abort_flag);
+            if (ok) {
+                const uint8_t *tile = smem + C::kFixedOff + h * C::kTileBytes;
+#pragma unroll
+                for (int cb = 0; cb < D / 64; ++cb) {
+                    const uint8_t *row = tile + cb * (BT * 128) + r * 128;
+                    uint32_t wv[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(row + ((c ^ (r & 7)) << 4));
+                        wv[4 * c] = v.x;
+                        wv[4 * c + 1] = v.y;
+                        wv[4 * c + 2] = v.z;
+                        wv[4 * c + 3] = v.w;
+                    }
+                    tmem_st32(tmem + lane_off + (h ? kColDO : kColQ) + cb * 32, wv);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_qtm);
+        }
         for (int n = 0; n < nsteps && ok; ++n) {
             const int u = 2 * n + hf;
             const uint32_t col = 128u * (u % NB) + 32u * w;

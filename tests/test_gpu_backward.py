@@ -52,9 +52,11 @@ def _check(name, got, ref):
                                    f"at {worst} (ref {r[worst]:.3e})")
 
 
+# 64: exactly one half-step; 192: the second tile's second half is empty; 300: a 44-row
+# tail inside the first half; 640: five steps, so the two- and three-stage rings wrap
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("N", [128, 300])
+@pytest.mark.parametrize("N", [64, 128, 192, 300, 640])
 def test_backward_small(d, causal, N):
     Q, K, V, dO = _inputs(2, 2, N, d, seed=300 + N + d)
     got = _gpu_backward(Q, K, V, dO, causal)

@@ -18,7 +18,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["fa_forward", "fa_forward_fp8", "fa_backward", "fa_backward_workspace_bytes", "fa_decode", "fa_decode_paged", "fa_decode_plan", "fa_decode_workspace_bytes",
+__all__ = ["fa_forward", "fa_forward_host", "fa_forward_host_workspace_bytes", "fa_forward_fp8", "fa_backward", "fa_backward_workspace_bytes", "fa_decode", "fa_decode_paged", "fa_decode_plan", "fa_decode_workspace_bytes",
            "fa_device_error", "FaError", "library", "library_path", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -55,6 +55,11 @@ def library():
         lib = ctypes.CDLL(_LIB_PATH)
         lib.fa_forward.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp]
         lib.fa_forward.restype = _i
+        lib.fa_forward_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _i,
+                                        _vp, ctypes.c_size_t, _vp]
+        lib.fa_forward_host.restype = _i
+        lib.fa_forward_host_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+        lib.fa_forward_host_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float, _i,
                                   _vp, ctypes.c_size_t, _vp]
         lib.fa_decode.restype = _i
@@ -153,6 +158,66 @@ def fa_forward(Q, K, V, causal=False, scale=None, key_len=None, out=None, lse=No
                               _ptr(key_len), _stream_handle(stream))
     if st != 0:
         raise FaError(st, "fa_forward")
+    return out, lse
+
+
+def _check_host_bf16(name, t):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) bfloat16 tensor")
+    if t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 4-D tensor")
+
+
+def fa_forward_host_workspace_bytes(B, H, N, d, heads_per_group=0):
+    """Device scratch bytes fa_forward_host needs (0 for an invalid shape)."""
+    return int(library().fa_forward_host_workspace_bytes(B, H, N, d, heads_per_group))
+
+
+def fa_forward_host(Q, K, V, causal=False, scale=None, key_len=None, out=None, lse=None, return_lse=True,
+                    heads_per_group=0, workspace=None, stream=None, device=None):
+    """fa_forward over HOST bf16 tensors [B, H, N, d]; returns host (O, L).
+
+    The library copies groups of heads to the device, runs the forward on each and
+    copies the results back, overlapping the copies of one group with the work of
+    the others.  Pinned inputs (and outputs: allocated pinned when Q is pinned) let
+    the copies run asynchronously; the results are complete once `stream` (the
+    current stream of `device` by default) is synchronised.  key_len: optional
+    host int32 [B]; workspace: optional CUDA uint8 scratch.
+    """
+    torch = _torch()
+    for n, t in (("Q", Q), ("K", K), ("V", V)):
+        _check_host_bf16(n, t)
+    if K.shape != Q.shape or V.shape != Q.shape:
+        raise ValueError("Q, K, V must share the shape [B, H, N, d]")
+    B, H, N, d = Q.shape
+    pin = Q.is_pinned()
+    if out is None:
+        out = torch.empty(Q.shape, dtype=torch.bfloat16, pin_memory=pin)
+    else:
+        _check_host_bf16("out", out)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    if lse is not None and (lse.is_cuda or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise TypeError("lse must be a contiguous host float32 tensor")
+    kl = None
+    if key_len is not None:
+        kl = torch.as_tensor(key_len, dtype=torch.int32).cpu().contiguous()
+        if kl.numel() != B:
+            raise ValueError("key_len must have B entries")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    need = library().fa_forward_host_workspace_bytes(B, H, N, d, heads_per_group)
+    if need == 0:
+        raise FaError(1, "fa_forward_host (shape or heads_per_group)")
+    if workspace is None:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    with torch.cuda.device(dev):
+        st = library().fa_forward_host(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), _ptr(lse), B, H, N, d,
+                                       int(bool(causal)), float(scale) if scale is not None else 0.0, _ptr(kl),
+                                       int(heads_per_group), _ptr(workspace), workspace.numel(),
+                                       _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, "fa_forward_host")
     return out, lse
 
 

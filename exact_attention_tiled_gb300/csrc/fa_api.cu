@@ -462,3 +462,161 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
 }
 
 }  // extern "C"
+
+namespace {
+
+// fa_forward_host: a group is `hg` consecutive heads of one batch element; a
+// slot holds one group's Q, K, V, O and L on the device.
+constexpr size_t kHostGroupBytes = 16u << 20;  // automatic group: Q slice <= 16 MiB
+constexpr int kHostSlots = 3;                  // groups in flight
+
+struct HostPlan {
+    int hg = 0;            // heads per group
+    int groups = 0;        // B * H / hg
+    int slots = 0;
+    size_t tile = 0;       // bytes of one group's Q (= K = V = O) slice, 256-aligned
+    size_t lrows = 0;      // bytes of one group's L slice, 256-aligned
+    size_t slot = 0;       // 4 * tile + lrows
+    size_t keylen = 0;     // device copy of key_len
+    size_t total = 0;
+};
+
+bool host_plan(int B, int H, int N, int d, int heads_per_group, HostPlan *pl) {
+    if (B < 1 || H < 1 || N < 1 || B > 65535 || H > 65535 || (d != 64 && d != 128)) return false;
+    if (static_cast<long long>(B) * H * N > (1ll << 40)) return false;
+    const size_t head = static_cast<size_t>(N) * d * 2;
+    int hg = heads_per_group;
+    if (hg == 0) {
+        hg = 1;
+        for (int c = 1; c <= H; ++c)
+            if (H % c == 0 && static_cast<size_t>(c) * head <= kHostGroupBytes) hg = c;
+    }
+    if (hg < 1 || hg > H || H % hg != 0) return false;
+    pl->hg = hg;
+    pl->groups = static_cast<int>(static_cast<long long>(B) * H / hg);
+    pl->slots = pl->groups < kHostSlots ? pl->groups : kHostSlots;
+    pl->tile = align256(static_cast<size_t>(hg) * head);
+    pl->lrows = align256(static_cast<size_t>(hg) * N * sizeof(float));
+    pl->slot = 4 * pl->tile + pl->lrows;
+    pl->keylen = align256(static_cast<size_t>(B) * sizeof(int32_t));
+    pl->total = pl->slots * pl->slot + pl->keylen;
+    return true;
+}
+
+// Internal streams and events of fa_forward_host, created once per device.
+struct HostStreams {
+    cudaStream_t st[kHostSlots];
+    cudaEvent_t start, keylen, done[kHostSlots];
+};
+
+cudaError_t host_streams(HostStreams **out) {
+    static std::mutex mu;
+    static HostStreams *per_dev[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!per_dev[dev]) {
+        HostStreams *h = new HostStreams;
+        for (int i = 0; i < kHostSlots && e == cudaSuccess; ++i) {
+            e = cudaStreamCreateWithFlags(&h->st[i], cudaStreamNonBlocking);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->done[i], cudaEventDisableTiming);
+        }
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->start, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->keylen, cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;   // (the partial set is leaked: creation failing is fatal anyway)
+        per_dev[dev] = h;
+    }
+    *out = per_dev[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_forward_host_workspace_bytes(int B, int H, int N, int d, int heads_per_group) {
+    HostPlan pl;
+    return host_plan(B, H, N, d, heads_per_group, &pl) ? pl.total : 0;
+}
+
+fa_status fa_forward_host(const void *Qh, const void *Kh, const void *Vh, void *Oh, float *Lh, int B, int H,
+                          int N, int d, int causal, float scale, const int32_t *key_len_host,
+                          int heads_per_group, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+    if (!Qh || !Kh || !Vh || !Oh) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * H * N > (1ll << 40)) return FA_ERR_UNSUPPORTED;
+    if (!(std::isfinite(scale))) return FA_ERR_INVALID_ARG;
+    HostPlan pl;
+    if (!host_plan(B, H, N, d, heads_per_group, &pl)) return FA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < pl.total || !aligned(workspace, 256)) return FA_ERR_WORKSPACE;
+    if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(d));
+
+    unsigned *err = nullptr;
+    fa_status s = error_word(&err);
+    if (s != FA_OK) return s;
+    HostStreams *hs = nullptr;
+    if (host_streams(&hs) != cudaSuccess) return FA_ERR_CUDA;
+    const cudaStream_t caller = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *kl_dev = key_len_host ? reinterpret_cast<int32_t *>(ws + pl.slots * pl.slot) : nullptr;
+
+    bool ok = cudaEventRecord(hs->start, caller) == cudaSuccess;
+    for (int i = 0; ok && i < pl.slots; ++i) ok = cudaStreamWaitEvent(hs->st[i], hs->start, 0) == cudaSuccess;
+    if (ok && kl_dev) {
+        ok = cudaMemcpyAsync(kl_dev, key_len_host, static_cast<size_t>(B) * sizeof(int32_t), cudaMemcpyHostToDevice,
+                             hs->st[0]) == cudaSuccess &&
+             cudaEventRecord(hs->keylen, hs->st[0]) == cudaSuccess;
+        for (int i = 1; ok && i < pl.slots; ++i) ok = cudaStreamWaitEvent(hs->st[i], hs->keylen, 0) == cudaSuccess;
+    }
+    const size_t head_elems = static_cast<size_t>(N) * d;
+    const size_t bytes = static_cast<size_t>(pl.hg) * head_elems * 2;
+    for (int g = 0; ok && g < pl.groups; ++g) {
+        // slot g % slots: its stream runs H2D(g), the kernel, D2H(g), then H2D(g + slots)
+        const int i = g % pl.slots;
+        const cudaStream_t st = hs->st[i];
+        uint8_t *slot = ws + i * pl.slot;
+        uint8_t *q = slot, *k = slot + pl.tile, *v = slot + 2 * pl.tile, *o = slot + 3 * pl.tile;
+        float *l = reinterpret_cast<float *>(slot + 4 * pl.tile);
+        const size_t bh0 = static_cast<size_t>(g) * pl.hg;   // first (batch, head) of the group
+        const int b = static_cast<int>(bh0 / H);
+        const size_t off = bh0 * head_elems * 2;
+        ok = cudaMemcpyAsync(q, static_cast<const uint8_t *>(Qh) + off, bytes, cudaMemcpyHostToDevice, st) ==
+                 cudaSuccess &&
+             cudaMemcpyAsync(k, static_cast<const uint8_t *>(Kh) + off, bytes, cudaMemcpyHostToDevice, st) ==
+                 cudaSuccess &&
+             cudaMemcpyAsync(v, static_cast<const uint8_t *>(Vh) + off, bytes, cudaMemcpyHostToDevice, st) ==
+                 cudaSuccess;
+        if (!ok) break;
+        PrefillParams p;
+        std::memset(&p, 0, sizeof p);
+        p.Q = q;
+        p.K = k;
+        p.V = v;
+        p.O = o;
+        p.L = Lh ? l : nullptr;
+        p.key_len = kl_dev ? kl_dev + b : nullptr;
+        p.B = 1;
+        p.H = pl.hg;
+        p.N = N;
+        p.causal = causal;
+        p.scale_log2 = scale * 1.4426950408889634f;
+        p.err = err;
+        ok = launch_prefill(p, d, st) == cudaSuccess &&
+             cudaMemcpyAsync(static_cast<uint8_t *>(Oh) + off, o, bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+        if (ok && Lh)
+            ok = cudaMemcpyAsync(Lh + bh0 * N, l, static_cast<size_t>(pl.hg) * N * sizeof(float),
+                                 cudaMemcpyDeviceToHost, st) == cudaSuccess;
+    }
+    // the caller's stream waits for every slot stream, also after a failure
+    bool joined = true;
+    for (int i = 0; i < pl.slots; ++i)
+        joined = cudaEventRecord(hs->done[i], hs->st[i]) == cudaSuccess &&
+                 cudaStreamWaitEvent(caller, hs->done[i], 0) == cudaSuccess && joined;
+    return ok && joined ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

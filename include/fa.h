@@ -93,6 +93,45 @@ FA_API fa_status fa_forward(const void *Q, const void *K, const void *V, void *O
                      const int32_t *key_len, fa_stream_t stream);
 
 /*
+ * fa_forward_host -- fa_forward over HOST buffers, with the host<->device
+ * copies inside the call.  The (batch, head) slices are independent problems
+ * ("Infra: Flash Attention", "Attention and its scope": each head attends on
+ * its own), so the call splits them into groups of `heads_per_group`
+ * consecutive heads of one batch element and pipelines, on internal streams,
+ * the copy of a group's Q, K, V to the device, fa_forward on it, and the copy
+ * of its O (and L) back, so that the copies of one group overlap the compute
+ * and copies of the others.  The results are bit-identical to fa_forward on
+ * the same data (every (batch, head) is computed by the same kernel code).
+ *
+ *   Qh, Kh, Vh  HOST bf16 [B, H, N, d], contiguous; page-locked (pinned)
+ *               memory lets the copies run asynchronously and overlap, other
+ *               host memory works but each copy then blocks the host.
+ *   Oh          HOST bf16 [B, H, N, d] output.
+ *   Lh          HOST float [B, H, N] output, or NULL.
+ *   key_len_host  NULL, or a HOST int32 [B] (read before the call returns).
+ *   heads_per_group  0 = automatic (the largest divisor of H whose Q slice
+ *               is at most 16 MiB); otherwise a divisor of H.
+ *   workspace   DEVICE scratch, 256-byte aligned, at least
+ *               fa_forward_host_workspace_bytes(B, H, N, d, heads_per_group)
+ *               bytes; it holds up to three groups' Q, K, V, O, L in flight.
+ *   stream      work is ordered after what `stream` already holds, and
+ *               `stream` waits for the whole call (the last copy to Oh/Lh)
+ *               before any later work; the host does not wait, so Oh and Lh
+ *               are complete once `stream` is synchronised.
+ * Other arguments and the arithmetic are those of fa_forward.
+ * Errors: FA_ERR_INVALID_ARG (null pointers, shapes, heads_per_group not
+ * dividing H), FA_ERR_UNSUPPORTED (d), FA_ERR_WORKSPACE, FA_ERR_CUDA (a copy
+ * or launch failed; some groups may then be missing from Oh).
+ */
+FA_API fa_status fa_forward_host(const void *Qh, const void *Kh, const void *Vh, void *Oh, float *Lh,
+                                 int B, int H, int N, int d, int causal, float scale,
+                                 const int32_t *key_len_host, int heads_per_group, void *workspace,
+                                 size_t workspace_bytes, fa_stream_t stream);
+
+/* Device scratch bytes fa_forward_host needs; 0 for an invalid shape. */
+FA_API size_t fa_forward_host_workspace_bytes(int B, int H, int N, int d, int heads_per_group);
+
+/*
  * fa_forward_fp8 -- fa_forward with FP8 (E4M3) inputs.  ("Infra: Flash
  * Attention", "FlashAttention-3": FA3 explores FP8 and its quantisation error
  * has to be evaluated on its own.)  The attention computed is exactly

@@ -235,3 +235,41 @@ def test_forward_fp8_rejects_bad_arguments_before_cuda(lib):
     assert f8(wsb=1024) == 4
     assert lib.fa_forward_fp8_workspace_bytes(1, 2, 300, 128) == (2 * 300 * 128 * 2 + 255) // 256 * 256
     assert lib.fa_forward_fp8_workspace_bytes(1, 2, 300, 64) == 0
+
+
+def test_forward_host_rejects_bad_arguments_before_cuda(lib):
+    def fh(**kw):
+        a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, L=None, B=2, H=6, N=300, d=64, causal=0, scale=0.0, kl=None,
+                 hpg=0, ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return lib.fa_forward_host(a["Q"], a["K"], a["V"], a["O"], a["L"], a["B"], a["H"], a["N"], a["d"],
+                                   a["causal"], ctypes.c_float(a["scale"]), a["kl"], a["hpg"], a["ws"], a["wsb"],
+                                   None)
+    assert fh(Q=None) == 1
+    assert fh(O=None) == 1
+    assert fh(N=0) == 1
+    assert fh(causal=2) == 1
+    assert fh(d=96) == 2
+    assert fh(hpg=4) == 1          # does not divide H = 6
+    assert fh(hpg=7) == 1
+    assert fh(ws=None) == 4
+    assert fh(ws=FAKE + 16) == 4   # not 256-byte aligned
+    assert fh(wsb=1024) == 4
+
+
+def test_forward_host_workspace_plan(lib):
+    ws = lib.fa_forward_host_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    a256 = lambda v: (v + 255) // 256 * 256
+    # automatic groups: the largest divisor of H whose Q slice is at most 16 MiB
+    head = 8192 * 128 * 2                       # 2 MiB per head
+    slot = 4 * a256(8 * head) + a256(8 * 8192 * 4)
+    assert ws(1, 32, 8192, 128, 0) == 3 * slot + 256
+    # explicit groups; fewer groups than slots use fewer slots
+    slot1 = 4 * a256(300 * 64 * 2) + a256(300 * 4)
+    assert ws(2, 6, 300, 64, 1) == 3 * slot1 + 256
+    slot6 = 4 * a256(6 * 300 * 64 * 2) + a256(6 * 300 * 4)
+    assert ws(1, 6, 300, 64, 6) == 1 * slot6 + 256
+    assert ws(2, 6, 300, 64, 6) == 2 * slot6 + 256
+    assert ws(2, 6, 300, 64, 4) == 0
+    assert ws(2, 6, 300, 96, 0) == 0

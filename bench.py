@@ -111,58 +111,90 @@ def replica_throughput(work_per_rank, ms_slowest, world):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock/throttle samples, 20 ms apart, time-stamped.
+
+    The sampler is started before the timed region and only its samples whose
+    time stamps fall between mark_start() and mark_end() are summarised."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, index):
         self.index = index
         self.proc = None
         self.file = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=self.file, stderr=subprocess.DEVNULL)
+            # do not start timing before the sampler produces rows (bounded wait)
+            deadline = time.time() + 10.0
+            while time.time() < deadline and os.path.getsize(self.file.name) == 0:
+                if self.proc.poll() is not None:
+                    break
+                time.sleep(0.02)
         except Exception:
             self.proc = None
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
     def __exit__(self, *a):
         if self.proc is not None:
+            time.sleep(2.5 * self.PERIOD_MS / 1000.0)  # let the last period's row land
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
 
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
     def summary(self):
         if self.proc is None or self.file is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.file.flush()
         with open(self.file.name) as f:
-            rows = [r.strip().split(",") for r in f if r.strip()]
+            rows = [[x.strip() for x in r.strip().split(",")] for r in f if r.strip()]
         os.unlink(self.file.name)
-        sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        parsed = []
         for r in rows:
-            r = [x.strip() for x in r]
-            if len(r) < 9:
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
+                parsed.append((self._stamp(r[0]), float(r[2]), float(r[3]),
+                               {n for n, v in zip(names, r[6:10]) if v.lower() == "active"}))
             except ValueError:
                 continue
-            for n, v in zip(names, r[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [x for x in parsed
+                  if x[0] is not None and self.t0 is not None and self.t1 is not None
+                  and self.t0 - 0.001 <= x[0] <= self.t1 + 0.001]
+        use = inside if inside else parsed
+        reasons = set().union(*(x[3] for x in use)) if use else set()
+        return {"sm_mhz": statistics.median([x[1] for x in use]) if use else None,
+                "sm_max_mhz": max(x[2] for x in use) if use else None,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "samples_window": "inside the timed region" if inside else
+                                  "none inside the timed region: all samples of the run"}
 
 
 # ------------------------------------------------------------------ our arm
@@ -216,6 +248,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
+        clk.mark_start()
         t_wall = time.perf_counter()
         for _ in range(args.steps):
             flush.fill_(1)
@@ -235,6 +268,7 @@ def run_ours(args, rank, world, local_rank):
             dc_ms.append(c.elapsed_time(d))
         torch.cuda.synchronize()
         wall = time.perf_counter() - t_wall
+        clk.mark_end()
     if world > 1:
         torch.distributed.barrier()
     clocks = clk.summary()
@@ -553,7 +587,7 @@ def run_profile_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

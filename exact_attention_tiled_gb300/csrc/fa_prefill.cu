@@ -45,6 +45,19 @@
 // tensor core executing one CTA's MMAs in issue order; and the barrier that
 // announces S_t(j+1) also covers PV_t(j), so the softmax may rescale O_t
 // as soon as it sees S_t(j+1).
+//
+// d = 64 runs a lookahead schedule instead.  TMEM then has room for P in
+// its own columns (S_0, S_1 [0,256), O_0, O_1 [256,384), P_0, P_1
+// [384,512)), so S_t(j+1) no longer has to wait for PV_t(j):
+//   * a softmax warp signals s_cons[t] as soon as S_t(j) is in its registers,
+//     and warp 1 then issues S_t(j+1), which runs during that softmax;
+//   * warp 2 issues PV_t(j) on p_ready[t] and commits pv_done[t];
+//   * the softmax waits for pv_done[t] (PV_t(j-1) complete) only before it
+//     stores P_t(j) or rescales O_t.
+// Each tile's next softmax step then starts as soon as the previous one ends,
+// instead of after its P V and S products.  S and P V come from two
+// issuing warps because one warp issuing all 24 MMAs of a KV step, on an
+// SMSP that also runs two softmax warps, falls behind.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -63,6 +76,7 @@ constexpr int BM = 128;          // query rows per tile (MMA M)
 constexpr int BN = 128;          // keys per KV tile (MMA N of Q K^T, K of P V)
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
+constexpr int kPvWarp = 2;           // P V issuer of the d = 64 lookahead schedule
 constexpr int kThreads = 384;        // 3 warpgroups: softmax 0, softmax 1, producer/MMA (+2 idle warps)
 constexpr int kRegsSoftmax = 216;    // per-thread registers of the softmax warpgroups after setmaxnreg
 constexpr int kRegsAux = 72;         // per-thread registers of the producer/MMA warpgroup
@@ -87,9 +101,12 @@ struct Cfg {
     static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
     // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_ready[2], o_final[2], mma_done,
     //           q_free, o_free[2]
-    static constexpr int kNumBars = 1 + 2 * kSlots + 10;
+    // d = 64 lookahead adds s_cons[2], pv_done[2] and the second issuer's mma_done
+    static constexpr int kNumBars = 1 + 2 * kSlots + 15;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;    // tmem base + abort flag
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // +1024 for base alignment
+    static constexpr uint32_t kPCol = 384;  // d = 64 lookahead: P_t at columns [384 + 64 t, 448 + 64 t)
+    static_assert(D != 64 || kPCol + 2 * 64 <= kTmemCols, "P_0, P_1 must fit beside S and O");
 };
 
 struct TmapSet {
@@ -195,6 +212,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_mma_done = bars + 8u * (7 + 2 * C::kSlots);
     const uint32_t bar_q_free = bars + 8u * (8 + 2 * C::kSlots);
     auto bar_o_free = [&](int t) { return bars + 8u * (9 + 2 * C::kSlots + t); };
+    auto bar_s_cons = [&](int t) { return bars + 8u * (11 + 2 * C::kSlots + t); };
+    auto bar_pv_done = [&](int t) { return bars + 8u * (13 + 2 * C::kSlots + t); };
+    const uint32_t bar_mma_done_pv = bars + 8u * (15 + 2 * C::kSlots);
+    // the d = 64 lookahead schedule (see the top of this file)
+    constexpr bool kLA = (D == 64) && !QK8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
@@ -214,8 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_p_ready(t), 4);
             mbar_init(bar_o_final(t), 1);
             mbar_init(bar_o_free(t), 4);
+            mbar_init(bar_s_cons(t), 4);
+            mbar_init(bar_pv_done(t), 1);
         }
         mbar_init(bar_mma_done, 1);
+        mbar_init(bar_mma_done_pv, 1);
         mbar_init(bar_q_free, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -311,10 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int item = first; item < g; ++item)
                     mbar_wait(bar_kv_full(item % C::kSlots), (item / C::kSlots) & 1, p.err, kSiteDrain);
             }
-        } else if (warp == kMmaWarp) {
-            // ================================================= MMA issuer
+        } else if (warp == kMmaWarp || (kLA && warp == kPvWarp)) {
+            // ================================================= MMA issuer(s)
             // The whole warp runs the loop (warp-uniform control flow and
-            // operands); one elected lane issues each MMA and commit.
+            // operands); one elected lane issues each MMA and commit.  With
+            // the lookahead schedule warp 1 issues the S products and warp 2
+            // the P V products; otherwise warp 1 issues both.
+            const bool do_s = !kLA || warp == kMmaWarp;
+            const bool do_pv = !kLA || warp == kPvWarp;
             bool issued_any = false;
             {
                 constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);
@@ -344,13 +373,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t vd = sdesc_sw128(vslot, BN * 128, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
-                        mma_ts_warp(tmem + 256 + t * D, tmem + t * 128 + kk * 8, vd + ((kk * 2048) >> 4), idesc_o,
+                        const uint32_t pcol = kLA ? C::kPCol + t * 64 : t * 128u;
+                        mma_ts_warp(tmem + 256 + t * D, tmem + pcol + kk * 8, vd + ((kk * 2048) >> 4), idesc_o,
                                (j > 0 || kk > 0) ? 1u : 0u);
                     }
                 };
                 int g = 0;                 // running ring index of this item's K_0
                 int qi = 0;                // items with work so far
                 int pcnt[2] = {0, 0};      // PV_t issued so far (phase of p_ready[t])
+                int scons[2] = {0, 0};     // s_cons[t] phases consumed (lookahead)
                 int uses[2] = {0, 0};      // items in which tile t had work (o_final / o_free phases)
                 bool ok = true;
                 for (int r = 0; ok; ++r) {
@@ -358,25 +389,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (k >= num_items) break;
                     const Item it = item_info(p, k, npairs, upb);
                     if (it.ntot == 0) continue;
-                    ok = wait_or_abort_warp(bar_q, qi & 1, p.err, kSiteQ, abort_flag);
-                    if (ok) ok = wait_or_abort_warp(bar_kv_full(g % C::kSlots), (g / C::kSlots) & 1, p.err, kSiteKvFull,
-                                               abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // S_t(0) may overwrite the previous item's P_t: its PV was issued earlier.
+                    if (do_s) {
+                        ok = wait_or_abort_warp(bar_q, qi & 1, p.err, kSiteQ, abort_flag);
+                        if (ok) ok = wait_or_abort_warp(bar_kv_full(g % C::kSlots), (g / C::kSlots) & 1, p.err,
+                                                        kSiteKvFull, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        // S_t(0) may overwrite the previous item's S_t / P_t: the softmax has
+                        // read its last S_t (lookahead: s_cons consumed) and its PV was issued.
 #pragma unroll
-                    for (int t = 0; t < 2; ++t)
-                        if (it.nkv[t] > 0) {
-                            issue_s(t, ring + (g % C::kSlots) * C::kTileBytes);
-                            mma_commit_warp(bar_s_full(t));
-                        }
+                        for (int t = 0; t < 2; ++t)
+                            if (it.nkv[t] > 0) {
+                                issue_s(t, ring + (g % C::kSlots) * C::kTileBytes);
+                                mma_commit_warp(bar_s_full(t));
+                            }
+                        if (it.ntot == 1) mma_commit_warp(bar_q_free);  // the item's last S MMA is issued
+                    }
                     issued_any = true;
-                    if (it.ntot == 1) mma_commit_warp(bar_q_free);  // the item's last S MMA is issued
                     for (int j = 0; ok && j < it.ntot; ++j) {
                         const int iv = g + 2 * j + 1, ik = g + 2 * j + 2;
                         const int sv = iv % C::kSlots, sk = ik % C::kSlots;
                         const uint32_t vslot = ring + sv * C::kTileBytes;
                         const uint32_t kslot = ring + sk * C::kTileBytes;
+                        if constexpr (kLA) {
+                            if (do_s) {
+                                // S_t(j+1) as soon as softmax t has S_t(j) in registers
+                                bool k_ready = false;
+#pragma unroll
+                                for (int t = 0; t < 2; ++t) {
+                                    if (!ok || j >= it.nkv[t]) continue;
+                                    ok = wait_or_abort_warp(bar_s_cons(t), scons[t] & 1, p.err, kSiteS, abort_flag);
+                                    if (!ok) break;
+                                    ++scons[t];
+                                    if (j + 1 < it.nkv[t]) {
+                                        if (!k_ready) {
+                                            ok = wait_or_abort_warp(bar_kv_full(sk), (ik / C::kSlots) & 1, p.err,
+                                                                    kSiteKvFull, abort_flag);
+                                            if (!ok) break;
+                                            k_ready = true;
+                                        }
+                                        tc_fence_after();
+                                        issue_s(t, kslot);
+                                        mma_commit_warp(bar_s_full(t));
+                                    }
+                                }
+                                if (ok && j + 2 == it.ntot) mma_commit_warp(bar_q_free);  // last S MMA of the item issued
+                            } else {
+                                ok = wait_or_abort_warp(bar_kv_full(sv), (iv / C::kSlots) & 1, p.err, kSiteKvFull,
+                                                        abort_flag);
+#pragma unroll
+                                for (int t = 0; t < 2; ++t) {
+                                    if (!ok || j >= it.nkv[t]) continue;
+                                    // O_t is overwritten by PV_t(0): the previous item's epilogue must have read it
+                                    if (j == 0 && uses[t] > 0) {
+                                        ok = wait_or_abort_warp(bar_o_free(t), (uses[t] - 1) & 1, p.err, kSiteO,
+                                                                abort_flag);
+                                        if (!ok) break;
+                                    }
+                                    ok = wait_or_abort_warp(bar_p_ready(t), pcnt[t] & 1, p.err, kSiteP, abort_flag);
+                                    if (!ok) break;
+                                    ++pcnt[t];
+                                    tc_fence_after();
+                                    issue_pv(t, vslot, j);
+                                    // the item's last PV_t is announced by o_final, the others by pv_done
+                                    mma_commit_warp(j + 1 == it.nkv[t] ? bar_o_final(t) : bar_pv_done(t));
+                                }
+                            }
+                            continue;
+                        }
                         ok = wait_or_abort_warp(bar_kv_full(sv), (iv / C::kSlots) & 1, p.err, kSiteKvFull, abort_flag);
                         bool k_ready = false;
 #pragma unroll
@@ -417,13 +497,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (issued_any) {
                     // every MMA issued above has completed before TMEM is released
-                    mma_commit_warp(bar_mma_done);
-                    mbar_wait(bar_mma_done, 0, p.err, kSiteMmaDone);
+                    const uint32_t bd = warp == kMmaWarp ? bar_mma_done : bar_mma_done_pv;
+                    mma_commit_warp(bd);
+                    mbar_wait(bd, 0, p.err, kSiteMmaDone);
                     __syncwarp();
                 }
             }
             __syncwarp();
-        }  // warps 2, 3: no role
+        }  // warp 3 (and warp 2 at d = 128): no role
     } else {
         setmaxnreg_inc<kRegsSoftmax>();
         // ================================================= softmax warpgroups
@@ -435,6 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t o_addr = tmem + lane_off + 256 + t * D;
         const float sl2 = p.scale_log2;
         int scnt = 0;   // S_t completions consumed (phase of s_full[t])
+        int pvcnt = 0;  // pv_done[t] phases consumed (lookahead)
+        const uint32_t p_addr = kLA ? tmem + lane_off + C::kPCol + t * 64 : s_addr;
         int uses = 0;   // items in which this tile had work (phase of o_final[t])
         int g = 0;      // running ring index of the item's K_0
         bool ok = true;
@@ -461,12 +544,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = __all_sync(0xffffffffu, wait_or_abort(bar_s_full(t), scnt & 1, p.err, kSiteS, abort_flag));
                 if (!ok) break;
                 ++scnt;
-                // S_t(j) complete implies every MMA issued before it is complete:
-                // the releasing tile (the one active in every KV step) hands K_j
-                // and V_{j-1} back to the producer with a plain arrive.
+                // S_t(j) complete implies every MMA its issuer issued before it is
+                // complete: the releasing tile (the one active in every KV step)
+                // hands K_j (and, with one issuer, V_{j-1}) back to the producer
+                // with a plain arrive.  With the lookahead schedule V_{j-1} is
+                // released below, once PV(j-1) is known complete.
                 if (t == it.t_rel && quarter == 0 && lane == 0) {
                     mbar_arrive(bar_kv_empty((g + 2 * j) % C::kSlots));
-                    if (j > 0) mbar_arrive(bar_kv_empty((g + 2 * j - 1) % C::kSlots));
+                    if (!kLA && j > 0) mbar_arrive(bar_kv_empty((g + 2 * j - 1) % C::kSlots));
                 }
                 tc_fence_after();
                 __syncwarp();
@@ -476,6 +561,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+                if constexpr (kLA) {
+                    // S_t(j) is in registers: S_t(j+1) may be written
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_s_cons(t));
+                }
 
                 // mask: keys beyond key_len / the sequence, and the causal future
                 const int kbase = j * BN;
@@ -522,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __nv_bfloat162 pr = __floats2bfloat162_rn(w.x, w.y);
                         pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&pr);
                     }
-                    // P columns 16c .. 16c+15 of this tile's S region
+                    // P columns 16c .. 16c+15 of this tile's P (over S, or its own columns at d = 64)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) sr[c][e] = pk[e];
                 }
@@ -535,8 +626,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         hi[e] = sr[2][e];
                         hi[16 + e] = sr[3][e];
                     }
-                    tmem_st32(s_addr + 0, lo);
-                    tmem_st32(s_addr + 32, hi);
+                    if (kLA && j > 0) {
+                        // PV_t(j-1) complete: P_t may be overwritten and O_t rescaled.  On the
+                        // releasing tile it also covers the other tile's PV(j-1), so V_{j-1} is free.
+                        ok = __all_sync(0xffffffffu,
+                                        wait_or_abort(bar_pv_done(t), pvcnt & 1, p.err, kSiteP, abort_flag));
+                        if (!ok) break;
+                        ++pvcnt;
+                        tc_fence_after();
+                        if (t == it.t_rel && quarter == 0 && lane == 0)
+                            mbar_arrive(bar_kv_empty((g + 2 * j - 1) % C::kSlots));
+                    }
+                    tmem_st32(p_addr + 0, lo);
+                    tmem_st32(p_addr + 32, hi);
                 }
                 const float2 s01 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
                 l_run = fmaf(l_run, alpha, s01.x + s01.y);

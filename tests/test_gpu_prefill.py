@@ -139,3 +139,31 @@ def test_forward_is_deterministic():
     a = _fwd(Q, K, V, True)
     b = _fwd(Q, K, V, True)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("B,H,N,causal,key_len", [
+    (1, 2, 128, False, None),          # one query tile: the second tile of the pair has no work
+    (2, 1, 200, True, [200, 0]),       # a partial second tile; a batch with no valid key
+    (1, 3, 256, True, None),           # two tiles with 1 and 2 KV steps
+    (2, 2, 1536, True, [1536, 700]),   # long causal items, uneven steps, key padding mid-item
+])
+def test_d64_schedule_edges(B, H, N, causal, key_len):
+    """d = 64 runs its own schedule (S of the next KV tile issued while the softmax of the
+    current one runs, P in separate tensor-memory columns, two issuing warps): items whose
+    two query tiles have different numbers of KV steps, a single tile, and empty rows."""
+    Q, K, V = workloads.prefill_inputs(B, H, N, 64, seed=N + 5 * B + H)
+    O, L = _fwd(Q, K, V, causal, key_len)
+    Oref, Lref = oracle.sdpa_forward(Q, K, V, causal=causal, key_len=key_len)
+    compare(f"d64 edges B{B} H{H} N{N} c{int(causal)} kl{key_len}", O, L, Oref, Lref)
+
+
+def test_d64_long_causal_many_rounds():
+    """B2 H16 N4096 d64 causal: 256 items of up to 32 KV steps over the persistent grid,
+    several rounds per CTA with heavy and light items mixed; whole heads against the oracle."""
+    B, H, N, d = 2, 16, 4096, 64
+    Q, K, V = workloads.prefill_inputs(B, H, N, d, seed=91)
+    O, L = _fwd(Q, K, V, True)
+    for b, h in ((0, 0), (1, 15)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        Oref, Lref = oracle.sdpa_forward(Q[sl], K[sl], V[sl], causal=True)
+        compare(f"d64 long causal b{b}h{h}", O[sl], L[sl], Oref, Lref)

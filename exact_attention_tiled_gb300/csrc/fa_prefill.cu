@@ -98,19 +98,25 @@ struct Cfg {
     static constexpr int kSlots = (D == 128) ? 4 : 8;         // KV ring slots (K and V alternate)
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = 2 * kTileBytes;
-    static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
+    // O staging for the TMA store of the epilogue: one buffer per query tile at
+    // d = 64, one shared by both tiles (they finish in turn) at d = 128
+    static constexpr int kOStageBufs = (D == 64) ? 2 : 1;
+    static constexpr int kOStageOff = kRingOff + kSlots * kTileBytes;
+    static constexpr int kBarOff = kOStageOff + kOStageBufs * kTileBytes;
     // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_ready[2], o_final[2], mma_done,
     //           q_free, o_free[2]
-    // d = 64 lookahead adds s_cons[2], pv_done[2] and the second issuer's mma_done
-    static constexpr int kNumBars = 1 + 2 * kSlots + 15;
+    // d = 64 lookahead adds s_cons[2], pv_done[2] and the second issuer's mma_done;
+    // the O staging adds ostage_full[2], ostage_free[2]
+    static constexpr int kNumBars = 1 + 2 * kSlots + 19;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;    // tmem base + abort flag
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // +1024 for base alignment
     static constexpr uint32_t kPCol = 384;  // d = 64 lookahead: P_t at columns [384 + 64 t, 448 + 64 t)
     static_assert(D != 64 || kPCol + 2 * 64 <= kTmemCols, "P_0, P_1 must fit beside S and O");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
 struct TmapSet {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, o;
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, unsigned *err, int site,
@@ -215,6 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_s_cons = [&](int t) { return bars + 8u * (11 + 2 * C::kSlots + t); };
     auto bar_pv_done = [&](int t) { return bars + 8u * (13 + 2 * C::kSlots + t); };
     const uint32_t bar_mma_done_pv = bars + 8u * (15 + 2 * C::kSlots);
+    auto bar_ostage_full = [&](int b) { return bars + 8u * (16 + 2 * C::kSlots + b); };
+    auto bar_ostage_free = [&](int b) { return bars + 8u * (18 + 2 * C::kSlots + b); };
     // the d = 64 lookahead schedule (see the top of this file)
     constexpr bool kLA = (D == 64) && !QK8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
@@ -238,6 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_o_free(t), 4);
             mbar_init(bar_s_cons(t), 4);
             mbar_init(bar_pv_done(t), 1);
+            mbar_init(bar_ostage_full(t), 4);
+            mbar_init(bar_ostage_free(t), 1);
         }
         mbar_init(bar_mma_done, 1);
         mbar_init(bar_mma_done_pv, 1);
@@ -517,6 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = p.scale_log2;
         int scnt = 0;   // S_t completions consumed (phase of s_full[t])
         int pvcnt = 0;  // pv_done[t] phases consumed (lookahead)
+        // O staging: buffer ob; its uses are counted in the order both warpgroups
+        // take them (tile 0, then tile 1, item by item)
+        const int ob = C::kOStageBufs == 2 ? t : 0;
+        const uint32_t ostage = sbase + C::kOStageOff + ob * C::kTileBytes;
+        int ouse = 0;   // uses of buffer ob before the current item
         const uint32_t p_addr = kLA ? tmem + lane_off + C::kPCol + t * 64 : s_addr;
         int uses = 0;   // items in which this tile had work (phase of o_final[t])
         int g = 0;      // running ring index of the item's K_0
@@ -696,11 +711,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_o_free(t));
-                if (store) {
+                // O goes out through shared memory and a TMA store: one thread per row
+                // writing its own 2d-byte row straight to global memory touches 32 cache
+                // lines per store instruction, which kept the epilogue (and the barrier
+                // polls queued behind those stores) slow.
+                const int ui = ouse + ((C::kOStageBufs == 1 && t == 1 && it.nkv[0] > 0) ? 1 : 0);
+                if (ui > 0) {
+                    ok = __all_sync(0xffffffffu, wait_or_abort(bar_ostage_free(ob), (ui - 1) & 1, p.err, kSiteO,
+                                                               abort_flag));
+                    if (!ok) break;
+                }
+                {
                     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             uint32_t w[4];
@@ -711,21 +735,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                           __uint_as_float(o[c][v * 8 + 2 * e + 1]) * inv);
                                 w[e] = *reinterpret_cast<const uint32_t *>(&pr);
                             }
-                            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                            // 16-byte chunk kc of row r in the 128-byte-swizzled layout of the O map
+                            const int kc = c * 4 + v;
+                            const uint32_t addr = ostage + (kc >> 3) * (BM * 128) + r * 128 +
+                                                  (static_cast<uint32_t>((kc & 7) ^ (r & 7)) << 4);
+                            st_shared_v4(addr, w[0], w[1], w[2], w[3]);
                         }
                     }
-                    if (p.L)
-                        p.L[static_cast<size_t>(it.bh) * N + qi] =
-                            l_run > 0.f ? (r_base + __log2f(l_run)) * kLn2 : -INFINITY;
                 }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_ostage_full(ob));
+                if (quarter == 0 && lane == 0) {
+                    // all four warps have staged their rows; rows past N are clipped by the store
+                    if (wait_or_abort(bar_ostage_full(ob), ui & 1, p.err, kSiteO, abort_flag)) {
+#pragma unroll
+                        for (int cb = 0; cb < D / 64; ++cb)
+                            tma_store_3d(&tm.o, ostage + cb * (BM * 128), cb * 64, my_row0, it.bh);
+                        bulk_commit_group();
+                        bulk_wait_group_read0();
+                    }
+                    mbar_arrive(bar_ostage_free(ob));
+                }
+                if (store && p.L)
+                    p.L[static_cast<size_t>(it.bh) * N + qi] =
+                        l_run > 0.f ? (r_base + __log2f(l_run)) * kLn2 : -INFINITY;
             } else if (store) {
                 // no valid key for this row (key_len = 0): O = 0, L = -inf
                 uint4 *dst = reinterpret_cast<uint4 *>(orow);
                 for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
                 if (p.L) p.L[static_cast<size_t>(it.bh) * N + qi] = -INFINITY;
             }
+            ouse += C::kOStageBufs == 2 ? (my_nkv > 0 ? 1 : 0) : (it.nkv[0] > 0 ? 1 : 0) + (it.nkv[1] > 0 ? 1 : 0);
             g += 2 * it.ntot;
         }
+        // the O stores this thread issued are complete before the CTA exits
+        if (quarter == 0 && lane == 0) bulk_wait_group0();
     }
 
     tc_fence_before();
@@ -742,7 +787,7 @@ cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
     const int BH = p.B * p.H;
     const bool maps = QK8 ? make_map_u8(&tm.q, p.Q, BH, p.N, D) && make_map_u8(&tm.k, p.K, BH, p.N, D)
                           : make_map(&tm.q, p.Q, BH, p.N, D) && make_map(&tm.k, p.K, BH, p.N, D);
-    if (!maps || !make_map(&tm.v, p.V, BH, p.N, D)) return cudaErrorInvalidValue;
+    if (!maps || !make_map(&tm.v, p.V, BH, p.N, D) || !make_map(&tm.o, p.O, BH, p.N, D)) return cudaErrorInvalidValue;
     const int smem = Cfg<D>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, QK8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

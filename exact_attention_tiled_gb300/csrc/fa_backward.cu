@@ -58,8 +58,14 @@ enum {
 };
 
 struct BwdMaps {
-    CUtensorMap q, k, v, dO;
+    CUtensorMap q, k, v, dO, dq, dk, dv;
 };
+
+// Row r, 16-byte chunk kc (8 bf16 columns) of a 128-row tile in the 128-byte
+// swizzled layout of the tensor maps (64-column blocks of 128 x 128 bytes).
+__device__ __forceinline__ uint32_t swz_chunk(uint32_t tile, int r, int kc) {
+    return tile + (kc >> 3) * (BT * 128) + r * 128 + (static_cast<uint32_t>((kc & 7) ^ (r & 7)) << 4);
+}
 
 __device__ __forceinline__ bool wait_abort(uint32_t bar, uint32_t parity, unsigned *err, int site,
                                            volatile int *abort_flag) {
@@ -430,13 +436,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
             __syncwarp();
         }
-        // tcgen05.ld is warp-collective: every lane loads, only rows < N store
+        // dV and dK are staged in the shared tiles K_j and V_j held (free once
+        // bar_done completed) and leave by TMA stores after the CTA's last barrier:
+        // one thread per key row storing its own row to global memory would touch
+        // 32 cache lines per store instruction.  Rows past N are clipped by the store.
         if (ok) {
-            const size_t row = (static_cast<size_t>(bh) * N + (key < N ? key : 0)) * D;
             {
-                // warpgroups 0, 1 write the two column halves of dV, warpgroups 2, 3 of dK
+                // warpgroups 0, 1 stage the two column halves of dV, warpgroups 2, 3 of dK
                 const int which = h >> 1;
-                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(which ? p.dK : p.dV) + row;
+                const uint32_t stage = which ? k_smem : v_smem;
                 const float mul = which ? p.scale : 1.f;
 #pragma unroll 1
                 for (int c = (h & 1) * (D / 64); c < (h & 1) * (D / 64) + D / 64; ++c) {
@@ -449,25 +457,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) a[e] = 0u;
                     }
-                    if (key < N) {
-                        uint4 *out = reinterpret_cast<uint4 *>(dst + c * 32);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            out[v] = make_uint4(
-                                pack_bf16(__uint_as_float(a[8 * v]) * mul, __uint_as_float(a[8 * v + 1]) * mul),
-                                pack_bf16(__uint_as_float(a[8 * v + 2]) * mul, __uint_as_float(a[8 * v + 3]) * mul),
-                                pack_bf16(__uint_as_float(a[8 * v + 4]) * mul, __uint_as_float(a[8 * v + 5]) * mul),
-                                pack_bf16(__uint_as_float(a[8 * v + 6]) * mul, __uint_as_float(a[8 * v + 7]) * mul));
-                    }
+                    for (int v = 0; v < 4; ++v)
+                        st_shared_v4(swz_chunk(stage, r, c * 4 + v),
+                                     pack_bf16(__uint_as_float(a[8 * v]) * mul, __uint_as_float(a[8 * v + 1]) * mul),
+                                     pack_bf16(__uint_as_float(a[8 * v + 2]) * mul, __uint_as_float(a[8 * v + 3]) * mul),
+                                     pack_bf16(__uint_as_float(a[8 * v + 4]) * mul, __uint_as_float(a[8 * v + 5]) * mul),
+                                     pack_bf16(__uint_as_float(a[8 * v + 6]) * mul, __uint_as_float(a[8 * v + 7]) * mul));
                     __syncwarp();   // reconverge before the next warp-collective load
                 }
             }
+            fence_proxy_async_shared();
         }
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (threadIdx.x == 0 && !*abort_flag) {
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb) {
+            tma_store_3d(&tm.dv, v_smem + cb * (BT * 128), cb * 64, key0, bh);
+            tma_store_3d(&tm.dk, k_smem + cb * (BT * 128), cb * 64, key0, bh);
+        }
+        bulk_commit_group();
+        bulk_wait_group0();
+    }
     if (warp == kMma) tmem_dealloc(tmem, 512);
 }
 
@@ -726,11 +741,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
             __syncwarp();
         }
-        // tcgen05.ld is warp-collective: every lane loads, only rows < N store
+        // dQ is staged in the shared tile Q_i held (free since Q_i was copied into
+        // TMEM) and leaves by TMA stores after the CTA's last barrier; rows past N
+        // are clipped by the store
         if (ok) {
-            __nv_bfloat16 *dst =
-                static_cast<__nv_bfloat16 *>(p.dQ) + (static_cast<size_t>(bh) * N + (q < N ? q : 0)) * D;
-            // warpgroup h writes dQ columns [32c, 32c + 32) for c = h, h + 4, ...
+            // warpgroup h stages dQ columns [32c, 32c + 32) for c = h, h + 4, ...
 #pragma unroll 1
             for (int c = h; c < D / 32; c += kComputeGroups) {
                 uint32_t a[32];
@@ -742,25 +757,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) a[e] = 0u;
                 }
-                if (q < N) {
-                    const float mul = p.scale;
-                    uint4 *out = reinterpret_cast<uint4 *>(dst + c * 32);
+                const float mul = p.scale;
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        out[v] = make_uint4(
-                            pack_bf16(__uint_as_float(a[8 * v]) * mul, __uint_as_float(a[8 * v + 1]) * mul),
-                            pack_bf16(__uint_as_float(a[8 * v + 2]) * mul, __uint_as_float(a[8 * v + 3]) * mul),
-                            pack_bf16(__uint_as_float(a[8 * v + 4]) * mul, __uint_as_float(a[8 * v + 5]) * mul),
-                            pack_bf16(__uint_as_float(a[8 * v + 6]) * mul, __uint_as_float(a[8 * v + 7]) * mul));
-                }
+                for (int v = 0; v < 4; ++v)
+                    st_shared_v4(swz_chunk(q_smem, r, c * 4 + v),
+                                 pack_bf16(__uint_as_float(a[8 * v]) * mul, __uint_as_float(a[8 * v + 1]) * mul),
+                                 pack_bf16(__uint_as_float(a[8 * v + 2]) * mul, __uint_as_float(a[8 * v + 3]) * mul),
+                                 pack_bf16(__uint_as_float(a[8 * v + 4]) * mul, __uint_as_float(a[8 * v + 5]) * mul),
+                                 pack_bf16(__uint_as_float(a[8 * v + 6]) * mul, __uint_as_float(a[8 * v + 7]) * mul));
                 __syncwarp();   // reconverge before the next warp-collective load
             }
+            fence_proxy_async_shared();
         }
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (threadIdx.x == 0 && !*abort_flag) {
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb) tma_store_3d(&tm.dq, q_smem + cb * (BT * 128), cb * 64, q0, bh);
+        bulk_commit_group();
+        bulk_wait_group0();
+    }
     if (warp == kMma) tmem_dealloc(tmem, 512);
 }
 
@@ -781,7 +800,9 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     std::memset(&tm, 0, sizeof tm);
     const int BH = p.B * p.H;
     if (!make_map(&tm.q, p.Q, BH, p.N, D) || !make_map(&tm.k, p.K, BH, p.N, D) ||
-        !make_map(&tm.v, p.V, BH, p.N, D) || !make_map(&tm.dO, p.dO, BH, p.N, D))
+        !make_map(&tm.v, p.V, BH, p.N, D) || !make_map(&tm.dO, p.dO, BH, p.N, D) ||
+        !make_map(&tm.dq, p.dQ, BH, p.N, D) || !make_map(&tm.dk, p.dK, BH, p.N, D) ||
+        !make_map(&tm.dv, p.dV, BH, p.N, D))
         return cudaErrorInvalidValue;
     const int smem = BwdCfg<D, HalfStepShape<D>::kStages>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -304,19 +304,21 @@ __global__ void __launch_bounds__(kSplitThreads) decode_split_kernel(const Decod
 }
 
 // ---------------------------------------------------------------------------
-// Merge kernel: grid (H, B); the log-sum-exp reduction of step 3, written as
-// the page writes it: first m = max_k m_k, then the l- and O-weighted sums.
+// Merge kernel: grid (H, B); the log-sum-exp reduction of step 3,
+//   m = max_k m_k,  l = sum_k l_k e^(m_k - m),  O = sum_k O_k l_k e^(m_k - m) / l,
+// evaluated as the pages' block-state merge ("Merging block states"): each warp
+// folds its chunks into a running (m, l, o) with a moving maximum, and the
+// warps' states are combined at the end with one shared maximum.  The result is
+// the same sum; no pass over the chunks waits for the global maximum first.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
     constexpr int kWarps = kMergeThreads / 32;
     constexpr int DPL = D / 32;  // dims per lane
-    __shared__ float red[kWarps];
+    __shared__ float wm[kWarps], wl[kWarps];
     __shared__ float accs[kWarps][D];
-    __shared__ float lsum[kWarps];
 
-    grid_dependency_wait();  // partials of the split kernel are visible after this
-
+    // the lengths are inputs: read them before waiting for the split kernel
     const int h = blockIdx.x, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int len = clamp_len(p.seqlens[b], p.Lmax);
@@ -325,53 +327,60 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     const float *ml = p.part_ml + bh * p.smax * 2;
     const float *po = p.part_o + bh * p.smax * D;
 
-    // m_f = max_k m_k over chunks with l_k > 0
-    float m = -INFINITY;
-    for (int k = threadIdx.x; k < n; k += kMergeThreads)
-        if (ml[2 * k + 1] > 0.f) m = fmaxf(m, ml[2 * k]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    float m_f = red[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) m_f = fmaxf(m_f, red[w]);
+    grid_dependency_wait();  // partials of the split kernel are visible after this
 
+    // this warp's chunks k = warp, warp + kWarps, ...: running maximum m (natural
+    // units), l = sum l_k e^(m_k - m), o = sum O_k l_k e^(m_k - m)
+    float m = -INFINITY, l = 0.f;
     float acc[DPL];
 #pragma unroll
     for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-    float l = 0.f;
-    if (m_f != -INFINITY) {
-        for (int k = warp; k < n; k += kWarps) {
-            const float lk = ml[2 * k + 1];
-            if (!(lk > 0.f)) continue;
-            const float wk = lk * __expf(ml[2 * k] - m_f);
-            l += wk;
-            const float *src = po + static_cast<size_t>(k) * D + lane * DPL;
-            if constexpr (DPL == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(src);
-                acc[0] = fmaf(wk, v.x, acc[0]);
-                acc[1] = fmaf(wk, v.y, acc[1]);
-                acc[2] = fmaf(wk, v.z, acc[2]);
-                acc[3] = fmaf(wk, v.w, acc[3]);
-            } else {
-                const float2 v = *reinterpret_cast<const float2 *>(src);
-                acc[0] = fmaf(wk, v.x, acc[0]);
-                acc[1] = fmaf(wk, v.y, acc[1]);
-            }
+#pragma unroll 2
+    for (int k = warp; k < n; k += kWarps) {
+        const float2 mlk = *reinterpret_cast<const float2 *>(ml + 2 * k);
+        float v[DPL];
+        const float *src = po + static_cast<size_t>(k) * D + lane * DPL;
+        if constexpr (DPL == 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(src);
+            v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+        } else {
+            const float2 t = *reinterpret_cast<const float2 *>(src);
+            v[0] = t.x; v[1] = t.y;
         }
+        if (!(mlk.y > 0.f)) continue;   // an empty chunk has weight 0
+        if (mlk.x > m) {
+            const float c = __expf(m - mlk.x);   // 0 while m = -inf
+            l *= c;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[e] *= c;
+            m = mlk.x;
+        }
+        const float wk = mlk.y * __expf(mlk.x - m);
+        l += wk;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk, v[e], acc[e]);
     }
 #pragma unroll
     for (int e = 0; e < DPL; ++e) accs[warp][lane * DPL + e] = acc[e];
-    if (lane == 0) lsum[warp] = l;
+    if (lane == 0) {
+        wm[warp] = m;
+        wl[warp] = l;
+    }
     __syncthreads();
 
     if (threadIdx.x < D) {
-        float l_f = 0.f, o = 0.f;
+        float m_f = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            l_f += lsum[w];
-            o += accs[w][threadIdx.x];
+        for (int w = 0; w < kWarps; ++w) m_f = fmaxf(m_f, wm[w]);
+        float l_f = 0.f, o = 0.f;
+        if (m_f != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                if (wm[w] == -INFINITY) continue;   // a warp without a non-empty chunk
+                const float c = __expf(wm[w] - m_f);
+                l_f = fmaf(wl[w], c, l_f);
+                o = fmaf(accs[w][threadIdx.x], c, o);
+            }
         }
         const float out = l_f > 0.f ? o / l_f : 0.f;
         static_cast<__nv_bfloat16 *>(p.O)[bh * D + threadIdx.x] = __float2bfloat16_rn(out);

@@ -78,8 +78,8 @@ constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kPvWarp = 2;           // P V issuer of the d = 64 lookahead schedule
 constexpr int kThreads = 384;        // 3 warpgroups: softmax 0, softmax 1, producer/MMA (+2 idle warps)
-constexpr int kRegsSoftmax = 216;    // per-thread registers of the softmax warpgroups after setmaxnreg
-constexpr int kRegsAux = 72;         // per-thread registers of the producer/MMA warpgroup
+constexpr int kRegsSoftmax = 208;    // per-thread registers of the softmax warpgroups after setmaxnreg
+constexpr int kRegsAux = 88;         // per-thread registers of the producer/MMA warpgroup (72 spilled its loop state)
 constexpr int kTmemCols = 512;
 constexpr long long kL2BlockBytes = 16ll << 20;  // K+V budget of a block of (batch, head) units
 constexpr int kPrefetchTiles = 4;   // L2 prefetch distance of the KV stream, in KV tiles

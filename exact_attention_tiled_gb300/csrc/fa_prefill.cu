@@ -31,8 +31,11 @@
 //     per query row.  They read S from TMEM, mask, update (m, l), write
 //     P = bf16(exp2(S*scale*log2e - m)) over the first half of S's TMEM
 //     columns, and rescale O in TMEM by alpha when some row's max moved.
-//     At the end they normalise O by 1/l and write O and L.
-//   Warps 0-3 form the first warpgroup (2 and 3 have no role); it hands
+//     At the end they normalise O by 1/l, stage it in shared memory in the
+//     layout of the O tensor map, and one thread stores the tile with TMA;
+//     each thread writes its L.
+//   Warps 0-3 form the first warpgroup (at d = 128 warps 2 and 3 have no
+//   role; at d = 64 warp 2 issues the P V products, see below); it hands
 //   registers to the softmax warpgroups with setmaxnreg so the softmax can
 //   hold a whole 128-column score row without spilling.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 after it.

@@ -504,9 +504,14 @@ bool host_plan(int B, int H, int N, int d, int heads_per_group, HostPlan *pl) {
 }
 
 // Internal streams and events of fa_forward_host, created once per device.
+// up copies every group's Q, K, V in, in group order, so the first group's
+// inputs are complete after one group's worth of copy time.  Slot stream
+// st[i] runs the kernel of each group that uses slot i and copies its O and L
+// out; the groups' kernels overlap across slots.  Per slot: h2d (inputs
+// landed), d2h (outputs left, the slot may be refilled).
 struct HostStreams {
-    cudaStream_t st[kHostSlots];
-    cudaEvent_t start, keylen, done[kHostSlots];
+    cudaStream_t up, st[kHostSlots];
+    cudaEvent_t start, h2d[kHostSlots], d2h[kHostSlots];
 };
 
 cudaError_t host_streams(HostStreams **out) {
@@ -519,12 +524,13 @@ cudaError_t host_streams(HostStreams **out) {
     std::lock_guard<std::mutex> lock(mu);
     if (!per_dev[dev]) {
         HostStreams *h = new HostStreams;
+        e = cudaStreamCreateWithFlags(&h->up, cudaStreamNonBlocking);
         for (int i = 0; i < kHostSlots && e == cudaSuccess; ++i) {
             e = cudaStreamCreateWithFlags(&h->st[i], cudaStreamNonBlocking);
-            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->done[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->h2d[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->d2h[i], cudaEventDisableTiming);
         }
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->start, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->keylen, cudaEventDisableTiming);
         if (e != cudaSuccess) return e;   // (the partial set is leaked: creation failing is fatal anyway)
         per_dev[dev] = h;
     }
@@ -564,32 +570,34 @@ fa_status fa_forward_host(const void *Qh, const void *Kh, const void *Vh, void *
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *kl_dev = key_len_host ? reinterpret_cast<int32_t *>(ws + pl.slots * pl.slot) : nullptr;
 
-    bool ok = cudaEventRecord(hs->start, caller) == cudaSuccess;
+    const cudaStream_t up = hs->up;
+    bool ok = cudaEventRecord(hs->start, caller) == cudaSuccess && cudaStreamWaitEvent(up, hs->start, 0) == cudaSuccess;
     for (int i = 0; ok && i < pl.slots; ++i) ok = cudaStreamWaitEvent(hs->st[i], hs->start, 0) == cudaSuccess;
-    if (ok && kl_dev) {
+    // the kernels read key_len after the first group's inputs, which follow it on `up`
+    if (ok && kl_dev)
         ok = cudaMemcpyAsync(kl_dev, key_len_host, static_cast<size_t>(B) * sizeof(int32_t), cudaMemcpyHostToDevice,
-                             hs->st[0]) == cudaSuccess &&
-             cudaEventRecord(hs->keylen, hs->st[0]) == cudaSuccess;
-        for (int i = 1; ok && i < pl.slots; ++i) ok = cudaStreamWaitEvent(hs->st[i], hs->keylen, 0) == cudaSuccess;
-    }
+                             up) == cudaSuccess;
     const size_t head_elems = static_cast<size_t>(N) * d;
     const size_t bytes = static_cast<size_t>(pl.hg) * head_elems * 2;
     for (int g = 0; ok && g < pl.groups; ++g) {
-        // slot g % slots: its stream runs H2D(g), the kernel, D2H(g), then H2D(g + slots)
+        // slot g % slots; each event is waited on before its next record (host order)
         const int i = g % pl.slots;
-        const cudaStream_t st = hs->st[i];
         uint8_t *slot = ws + i * pl.slot;
         uint8_t *q = slot, *k = slot + pl.tile, *v = slot + 2 * pl.tile, *o = slot + 3 * pl.tile;
         float *l = reinterpret_cast<float *>(slot + 4 * pl.tile);
         const size_t bh0 = static_cast<size_t>(g) * pl.hg;   // first (batch, head) of the group
         const int b = static_cast<int>(bh0 / H);
         const size_t off = bh0 * head_elems * 2;
-        ok = cudaMemcpyAsync(q, static_cast<const uint8_t *>(Qh) + off, bytes, cudaMemcpyHostToDevice, st) ==
+        // inputs: after the slot's previous outputs have left
+        if (g >= pl.slots) ok = cudaStreamWaitEvent(up, hs->d2h[i], 0) == cudaSuccess;
+        ok = ok &&
+             cudaMemcpyAsync(q, static_cast<const uint8_t *>(Qh) + off, bytes, cudaMemcpyHostToDevice, up) ==
                  cudaSuccess &&
-             cudaMemcpyAsync(k, static_cast<const uint8_t *>(Kh) + off, bytes, cudaMemcpyHostToDevice, st) ==
+             cudaMemcpyAsync(k, static_cast<const uint8_t *>(Kh) + off, bytes, cudaMemcpyHostToDevice, up) ==
                  cudaSuccess &&
-             cudaMemcpyAsync(v, static_cast<const uint8_t *>(Vh) + off, bytes, cudaMemcpyHostToDevice, st) ==
-                 cudaSuccess;
+             cudaMemcpyAsync(v, static_cast<const uint8_t *>(Vh) + off, bytes, cudaMemcpyHostToDevice, up) ==
+                 cudaSuccess &&
+             cudaEventRecord(hs->h2d[i], up) == cudaSuccess;
         if (!ok) break;
         PrefillParams p;
         std::memset(&p, 0, sizeof p);
@@ -605,17 +613,20 @@ fa_status fa_forward_host(const void *Qh, const void *Kh, const void *Vh, void *
         p.causal = causal;
         p.scale_log2 = scale * 1.4426950408889634f;
         p.err = err;
-        ok = launch_prefill(p, d, st) == cudaSuccess &&
+        const cudaStream_t st = hs->st[i];
+        ok = cudaStreamWaitEvent(st, hs->h2d[i], 0) == cudaSuccess && launch_prefill(p, d, st) == cudaSuccess &&
              cudaMemcpyAsync(static_cast<uint8_t *>(Oh) + off, o, bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess;
         if (ok && Lh)
             ok = cudaMemcpyAsync(Lh + bh0 * N, l, static_cast<size_t>(pl.hg) * N * sizeof(float),
                                  cudaMemcpyDeviceToHost, st) == cudaSuccess;
+        if (ok) ok = cudaEventRecord(hs->d2h[i], st) == cudaSuccess;
     }
-    // the caller's stream waits for every slot stream, also after a failure
-    bool joined = true;
+    // the caller's stream waits for every internal stream, also after a failure
+    bool joined = cudaEventRecord(hs->h2d[0], up) == cudaSuccess &&
+                  cudaStreamWaitEvent(caller, hs->h2d[0], 0) == cudaSuccess;
     for (int i = 0; i < pl.slots; ++i)
-        joined = cudaEventRecord(hs->done[i], hs->st[i]) == cudaSuccess &&
-                 cudaStreamWaitEvent(caller, hs->done[i], 0) == cudaSuccess && joined;
+        joined = cudaEventRecord(hs->d2h[i], hs->st[i]) == cudaSuccess &&
+                 cudaStreamWaitEvent(caller, hs->d2h[i], 0) == cudaSuccess && joined;
     return ok && joined ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -134,6 +134,20 @@ def test_many_short_items_persistent_rounds():
             compare(f"many items b{b}h{h} c{int(causal)}", O[sl], L[sl], Oref, Lref)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_items_d128_shared_output_staging(causal):
+    """B8 H32 N384 d128: 384 work items, so every CTA runs several items and both query
+    tiles of each item hand their output tile through the one shared-memory staging
+    buffer in turn; whole heads against the oracle."""
+    B, H, N, d = 8, 32, 384, 128
+    Q, K, V = workloads.prefill_inputs(B, H, N, d, seed=79)
+    O, L = _fwd(Q, K, V, causal)
+    for b, h in ((0, 0), (3, 17), (7, 31)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        Oref, Lref = oracle.sdpa_forward(Q[sl], K[sl], V[sl], causal=causal)
+        compare(f"d128 items b{b}h{h} c{int(causal)}", O[sl], L[sl], Oref, Lref)
+
+
 def test_forward_is_deterministic():
     Q, K, V = workloads.prefill_inputs(1, 8, 2048, 128, seed=78)
     a = _fwd(Q, K, V, True)

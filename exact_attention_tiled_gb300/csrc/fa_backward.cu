@@ -383,20 +383,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float *dv = lv + BT;              // D_i
             // masking only where the tile touches key_len, the sequence end or the diagonal
             const bool need_mask = key0 + BT > klen || q0 + BT > N || (p.causal && key0 + BT - 1 > q0);
-            // P^T and dS^T of the 32-column chunk c from its S^T and dP^T values
-            auto chunk = [&](int c, uint32_t (&sr)[32], const uint32_t (&dr)[32], uint32_t (&pp)[16],
-                             uint32_t (&dp)[16]) {
+            // P^T and dS^T of half hb (16 columns) of the 32-column chunk c from its S^T
+            // and dP^T values, into words 8 hb .. 8 hb + 7 of pp and dp
+            auto half = [&](int c, int hb, uint32_t (&sr)[16], const uint32_t (&dr)[16], uint32_t (&pp)[16],
+                            uint32_t (&dp)[16]) {
                 if (need_mask) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int q = q0 + c * 32 + e;
+                    for (int e = 0; e < 16; ++e) {
+                        const int q = q0 + c * 32 + hb * 16 + e;
                         if (!(key_ok && q < N && (!p.causal || key <= q))) sr[e] = __float_as_uint(-INFINITY);
                     }
                 }
-                const float4 *l4 = reinterpret_cast<const float4 *>(lv + c * 32);
-                const float4 *d4 = reinterpret_cast<const float4 *>(dv + c * 32);
+                const float4 *l4 = reinterpret_cast<const float4 *>(lv + c * 32 + hb * 16);
+                const float4 *d4 = reinterpret_cast<const float4 *>(dv + c * 32 + hb * 16);
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
+                for (int e = 0; e < 16; e += 4) {
                     const float4 lq = l4[e >> 2], dq = d4[e >> 2];
                     const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl22,
                                                  make_float2(-lq.x, -lq.y));
@@ -407,22 +408,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         __fmul2_rn(p0, make_float2(__uint_as_float(dr[e]) - dq.x, __uint_as_float(dr[e + 1]) - dq.y));
                     const float2 g1 =
                         __fmul2_rn(p1, make_float2(__uint_as_float(dr[e + 2]) - dq.z, __uint_as_float(dr[e + 3]) - dq.w));
-                    pp[e >> 1] = pack_bf16(p0.x, p0.y);
-                    pp[(e >> 1) + 1] = pack_bf16(p1.x, p1.y);
-                    dp[e >> 1] = pack_bf16(g0.x, g0.y);
-                    dp[(e >> 1) + 1] = pack_bf16(g1.x, g1.y);
+                    pp[8 * hb + (e >> 1)] = pack_bf16(p0.x, p0.y);
+                    pp[8 * hb + (e >> 1) + 1] = pack_bf16(p1.x, p1.y);
+                    dp[8 * hb + (e >> 1)] = pack_bf16(g0.x, g0.y);
+                    dp[8 * hb + (e >> 1) + 1] = pack_bf16(g1.x, g1.y);
                 }
             };
-            // this warpgroup's S^T and dP^T columns; P^T and dS^T are packed over the
-            // first 16 of them
-            uint32_t sr[32], dr[32];
-            tmem_ld32(tmem + lane_off + col, sr);
-            tmem_ld32(tmem + lane_off + col + 64, dr);
+            // this warpgroup's S^T and dP^T columns, in two halves of 16 so that only
+            // half of them is live at once (the second half loads while the first is
+            // computed); P^T and dS^T are packed over the first 16 of the 32 columns
+            uint32_t sa[16], da[16], sb[16], db[16];
+            tmem_ld16(tmem + lane_off + col, sa);
+            tmem_ld16(tmem + lane_off + col + 64, da);
             tmem_wait_ld();
-            reg_fence(sr);
-            reg_fence(dr);
+            reg_fence(sa);
+            reg_fence(da);
+            tmem_ld16(tmem + lane_off + col + 16, sb);
+            tmem_ld16(tmem + lane_off + col + 64 + 16, db);
             uint32_t pp[16], dp[16];
-            chunk(h, sr, dr, pp, dp);
+            half(h, 0, sa, da, pp, dp);
+            tmem_wait_ld();
+            reg_fence(sb);
+            reg_fence(db);
+            half(h, 1, sb, db, pp, dp);
             tmem_st16(tmem + lane_off + col, pp);
             tmem_st16(tmem + lane_off + col + 64, dp);
             tmem_wait_st();

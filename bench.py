@@ -559,6 +559,12 @@ def run_profile_case(args):
         wp = workloads.WORKLOADS[PREFILL]
         Q, K, V = workloads.prefill_inputs(wp.B, wp.H, wp.N, wp.d, wp.seed, device=dev)
         run = lambda: fa.fa_forward(Q, K, V, causal=True)
+    elif args.profile == "prefill_fp8":
+        wp = workloads.WORKLOADS[PREFILL]
+        Q, K, V = workloads.prefill_inputs(wp.B, wp.H, wp.N, wp.d, wp.seed, device=dev)
+        Q8, K8, V8 = (t.float().to(torch.float8_e4m3fn) for t in (Q, K, V))
+        ws8 = torch.empty(fa.fa_forward_fp8_workspace_bytes(wp.B, wp.H, wp.N, wp.d), device=dev, dtype=torch.uint8)
+        run = lambda: fa.fa_forward_fp8(Q8, K8, V8, causal=True, workspace=ws8)
     elif args.profile == "prefill64":
         # the batched d64 shape (B8 H16 N2048, x0.5): 192 MiB of inputs, more than L2
         w3 = workloads.WORKLOADS["prefill_b8h16_n2048_d64"]
@@ -596,7 +602,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["prefill", "prefill64", "decode", "backward"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "prefill64", "prefill_fp8", "decode", "backward"], default=None,
                     help="only launch one kernel warmup+steps times (for ncu captures)")
     ap.add_argument("--record-traffic", nargs=3, metavar=("REPORT", "KERNEL", "NOTE"), default=None,
                     help="write DRAM bytes per launch of KERNEL from an ncu report to profiles/")

@@ -119,7 +119,19 @@ void plan_decode(int B, int H, int Lmax, int num_splits, const int32_t *seqlens_
     }
     if (slots < 1) slots = 1;
     int c;
-    if (min_len == max_len) {
+    if (min_len == max_len && static_cast<long long>(B) * H * 20 <= 17ll * slots) {
+        // equal lengths and room for at least one chunk per sequence in 85 % of the
+        // slots: one wave of as many chunks (>= 256 tokens each) as fit in 85 % of
+        // the slots.  Measured on B1 H32 L32768 at 3 CTAs per SM: one wave of 256 to
+        // 384 CTAs streams 5.85-5.96 TB/s, a full wave (448) 5.78, and a partial
+        // second wave (512 or 608 CTAs) 4.8-5.4.
+        const long long units = static_cast<long long>(B) * H;
+        long long s_fit = (17ll * slots) / (20 * units);
+        const long long s_len = (max_len + 4 * kDecodeGranule - 1) / (4 * kDecodeGranule);
+        if (s_fit > s_len) s_fit = s_len;
+        if (s_fit < 1) s_fit = 1;
+        c = round_up((max_len + s_fit - 1) / s_fit, kDecodeGranule);
+    } else if (min_len == max_len) {
         const long long units = static_cast<long long>(B) * H;
         const int max_s = (max_len + kDecodeGranule - 1) / kDecodeGranule;
         double best = 1e300;
@@ -211,7 +223,7 @@ fa_status fa_decode_plan(int B, int H, int Lmax, int d, int num_splits, const in
     if (num_splits > 0) {
         // a fixed chunk count needs no device information
     } else if (num_sms > 0) {
-        slots = num_sms * 2;
+        slots = num_sms * 3;   // the split kernel's two-stage ring fits three CTAs per SM
     } else {
         int sms = 0, per = 0;
         fa_status s = device_sm_count(&sms);

@@ -27,7 +27,7 @@
 namespace fa {
 namespace {
 
-constexpr int kStages = 3;           // ring depth (2 x 32 KB per stage at d = 128)
+constexpr int kStages = 2;           // ring depth (2 x 32 KB per stage at d = 128): 3 CTAs per SM
 constexpr int kConsumerWarps = 4;
 constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMergeThreads = 256;

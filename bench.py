@@ -491,6 +491,71 @@ def oracle_sample(seconds_target, seed=0):
     return w / t / 1e12, threads, f"{nrows} random query rows of {PREFILL} ({w:.3e} FLOP in {t:.1f} s)"
 
 
+def host_cpu():
+    """Model name of the host CPU and the cores this process may run on."""
+    model = None
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                key, val = key.strip(), val.strip()
+                if key and val and key not in fields:
+                    fields[key] = val
+    except OSError:
+        pass
+    for key in ("model name", "Model", "Hardware"):
+        if key in fields:
+            model = fields[key]
+            break
+    if model is None and "CPU implementer" in fields:
+        model = f"implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    import platform
+    try:
+        affinity = len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        affinity = os.cpu_count() or 1
+    return {"cpu_model": model or platform.processor() or platform.machine(),
+            "machine": platform.machine(), "affinity_cores": affinity}
+
+
+def oracle_decode_rate(q, Kc, Vc, seqlens, threads):
+    """GB/s of cached K and V the float64 oracle attends per second (no split)."""
+    import oracle
+    H, d = int(q.shape[1]), int(q.shape[2])
+    nbytes = decode_bytes(H, [int(n) for n in seqlens], d)
+    t0 = time.perf_counter()
+    oracle.decode(q, Kc, Vc, seqlens, nthreads=threads)
+    return nbytes / max(time.perf_counter() - t0, 1e-9) / 1e9
+
+
+def oracle_extras(threads):
+    """The oracle on the whole decode workload (all threads and one thread) and
+    on the tiny prefill case (one thread), beside the sampled prefill rate."""
+    import oracle
+    from exact_attention_tiled_gb300 import workloads
+
+    out = host_cpu()
+    w = workloads.make(DECODE)
+    out["decode"] = {
+        "workload": DECODE, "unit": "GB/s",
+        "value": oracle_decode_rate(w["q"], w["Kc"], w["Vc"], w["seqlens"], threads), "cores": threads,
+        "value_1_thread": oracle_decode_rate(w["q"], w["Kc"], w["Vc"], w["seqlens"], 1),
+    }
+    del w
+    t = workloads.make("tiny_n256_d64")
+    wt = workloads.WORKLOADS["tiny_n256_d64"]
+    flops = prefill_flops(wt.B, wt.H, wt.N, wt.d, wt.causal)
+    tiny = {"workload": "tiny_n256_d64", "unit": "ms"}
+    for key, n in (("ms", threads), ("ms_1_thread", 1)):
+        t0 = time.perf_counter()
+        oracle.sdpa_forward(t["Q"], t["K"], t["V"], causal=wt.causal, nthreads=n)
+        tiny[key] = (time.perf_counter() - t0) * 1e3
+    tiny["tflops_1_thread"] = flops / (tiny["ms_1_thread"] * 1e-3) / 1e12
+    out["tiny"] = tiny
+    return out
+
+
 def run_reference(args):
     per_step = max(1.0, 150.0 / max(1, args.steps + args.warmup))
     vals = []
@@ -517,7 +582,7 @@ def run_reference(args):
         "data": "synthetic",
         "config": {"workload": PREFILL, "B": 1, "H": 32, "N": 8192, "d": 128, "causal": True, "seed": 2},
         "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": f"per step: {desc}"},
+                         "sample": f"per step: {desc}", **oracle_extras(threads)},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -632,7 +697,7 @@ def main():
     if rank == 0:
         v, threads, desc = oracle_sample(args.cpu_seconds)
         res["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                               "sample": desc}
+                               "sample": desc, **oracle_extras(threads)}
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch

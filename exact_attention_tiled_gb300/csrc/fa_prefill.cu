@@ -573,10 +573,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 __syncwarp();
+                // S_t(j) row into registers; the load also reduces the row to its
+                // maximum (tcgen05.ld.red), so unmasked tiles need no max pass.
+                // One 128-column load at d = 64, four 32-column loads at d = 128
+                // (the faster register allocation of each, measured).
                 uint32_t sr[4][32];
+                float hmax;
+                if constexpr (D == 64) {
+                    hmax = tmem_ld128_max(s_addr, reinterpret_cast<uint32_t (&)[128]>(sr));
+                    tmem_wait_ld();
+                    reg_fence_f(hmax);
+                } else {
+                    float hm[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
-                tmem_wait_ld();
+                    for (int c = 0; c < 4; ++c) hm[c] = tmem_ld32_max(s_addr + c * 32, sr[c]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) reg_fence_f(hm[c]);
+                    hmax = fmaxf(fmaxf(hm[0], hm[1]), fmaxf(hm[2], hm[3]));
+                }
 #pragma unroll
                 for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
                 if constexpr (kLA) {
@@ -598,15 +613,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 32; ++e)
                             if (c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
                 }
-                // row max: four independent chains of three-input maxima
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                // row max: from the load, or, on a tile with masked entries, over the
+                // masked row in four independent chains of three-input maxima
+                float mrow = hmax;
+                if (need_mask) {
+                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2)
-                        mx[(e >> 1) & 3] = fmax3(mx[(e >> 1) & 3], __uint_as_float(sr[c][e]),
-                                                 __uint_as_float(sr[c][e + 1]));
-                const float mrow = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+                        for (int e = 0; e < 32; e += 2)
+                            mx[(e >> 1) & 3] = fmax3(mx[(e >> 1) & 3], __uint_as_float(sr[c][e]),
+                                                     __uint_as_float(sr[c][e + 1]));
+                    mrow = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                }
+                mrow *= sl2;
                 const bool resc = mrow > r_base + kRescaleLog2;   // always true on the first valid tile
                 const float r_new = resc ? mrow : r_base;
                 // a row that has seen no valid key keeps a finite base, so no

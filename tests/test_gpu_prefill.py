@@ -121,6 +121,31 @@ def test_late_max_jump_rebases_and_rescales(d, causal):
     compare(f"max jump d{d} c{int(causal)}", O, L, Oref, Lref)
 
 
+@pytest.mark.parametrize("d,causal", [(64, False), (128, False), (64, True), (128, True)])
+def test_masked_keys_with_huge_scores_do_not_set_the_row_max(d, causal):
+    """Masked keys whose scores exceed every valid score by ~150 log2 units or more:
+    padded keys beyond key_len, or, causal, the last key of every 128-key tile, a
+    future key for the other rows of its tile.  The TMEM load's row maximum covers
+    the masked columns too, so a tile with masked entries must take its maximum over
+    the masked row; with the load's maximum every valid weight of such a row would
+    underflow to zero and O, L would be wrong."""
+    B, H, N = 2, 2, 640
+    Q, K, V = workloads.prefill_inputs(B, H, N, d, seed=91)
+    Qf = Q.float() * 0.5 + 1.0     # a positive mean along every dimension
+    Kf = K.float() * 0.5
+    key_len = None
+    if causal:
+        Kf[:, :, 127::128] = 16.0
+    else:
+        key_len = [400, 577]
+        for b, kl in enumerate(key_len):
+            Kf[b, :, kl:] = 16.0
+    Q, K = Qf.to(torch.bfloat16), Kf.to(torch.bfloat16)
+    O, L = _fwd(Q, K, V, causal, key_len)
+    Oref, Lref = oracle.sdpa_forward(Q, K, V, causal=causal, key_len=key_len)
+    compare(f"masked huge keys d{d} c{int(causal)}", O, L, Oref, Lref)
+
+
 def test_many_short_items_persistent_rounds():
     """B16 H32 N384: 1536 work items over the persistent grid (several rounds per CTA); every
     row of a few heads against the oracle."""

@@ -86,6 +86,12 @@ constexpr int kRegsAux = 88;         // per-thread registers of the producer/MMA
 constexpr int kTmemCols = 512;
 constexpr long long kL2BlockBytes = 16ll << 20;  // K+V budget of a block of (batch, head) units
 constexpr int kPrefetchTiles = 4;   // L2 prefetch distance of the KV stream, in KV tiles
+// At d = 64 the next item's Q and first kPrefetchTiles K/V tiles are prefetched
+// into L2 this many KV steps before the current item ends (d64 +3 %, measured);
+// at d = 128 (long causal items) the Q prefetch stays at the item's start and
+// the first K/V tiles at the next item's start (measured: no gain there).
+template <int D>
+constexpr int kNextItemPrefetchSteps = D == 64 ? 8 : 0;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleLog2 = 8.0f;  // move the exponent base only when the max grows by > 2^8
 
@@ -288,8 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const Item it = item_info(p, k, npairs, upb);
                     if (it.ntot == 0) continue;
                     // Q of the next item of this CTA: warm L2 while this one runs
+                    constexpr int kNextPf = kNextItemPrefetchSteps<D>;
                     const int kn = item_of_round(r + 1, G, cta);
-                    if (kn < num_items) {
+                    if (kNextPf == 0 && kn < num_items) {
                         const Item nx = item_info(p, kn, npairs, upb);
 #pragma unroll
                         for (int t = 0; t < 2; ++t)
@@ -308,13 +315,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         it.row0[t],
                                         it.bh, bar_q, pol_q);
                     ++qi;
-                    for (int j = 0; j < kPrefetchTiles && j < it.ntot; ++j)
+                    // this item's first K/V tiles (unless the previous item prefetched them)
+                    if (kNextPf == 0 || qi == 1)
+                        for (int j = 0; j < kPrefetchTiles && j < it.ntot; ++j)
 #pragma unroll
-                        for (int cb = 0; cb < C::kColBlocks; ++cb) {
-                            if (cb < kQKBlocks) tma_prefetch_3d(&tm.k, cb * kQKBlockElems, j * BN, it.bh);
-                            tma_prefetch_3d(&tm.v, cb * 64, j * BN, it.bh);
-                        }
+                            for (int cb = 0; cb < C::kColBlocks; ++cb) {
+                                if (cb < kQKBlocks) tma_prefetch_3d(&tm.k, cb * kQKBlockElems, j * BN, it.bh);
+                                tma_prefetch_3d(&tm.v, cb * 64, j * BN, it.bh);
+                            }
                     for (int j = 0; ok && j < it.ntot; ++j) {
+                        if (kNextPf > 0 && j == (it.ntot > kNextPf ? it.ntot - kNextPf : 0) && kn < num_items) {
+                            // the next item's Q and first K/V tiles, a few steps before this item ends
+                            const Item nx = item_info(p, kn, npairs, upb);
+#pragma unroll
+                            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                                for (int cb = 0; cb < kQKBlocks; ++cb)
+                                    tma_prefetch_3d(&tm.q, cb * kQKBlockElems, nx.row0[t], nx.bh);
+                            for (int jj = 0; jj < kPrefetchTiles && jj < nx.ntot; ++jj)
+#pragma unroll
+                                for (int cb = 0; cb < C::kColBlocks; ++cb) {
+                                    if (cb < kQKBlocks) tma_prefetch_3d(&tm.k, cb * kQKBlockElems, jj * BN, nx.bh);
+                                    tma_prefetch_3d(&tm.v, cb * 64, jj * BN, nx.bh);
+                                }
+                        }
                         for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
                             const int s = g % C::kSlots;
                             if (g >= C::kSlots &&

@@ -55,6 +55,27 @@ def test_fp8_forward_key_padding_and_empty_rows():
     assert np.all(O[2] == 0) and np.all(np.isneginf(L[2]))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_masked_keys_with_huge_scores_do_not_set_the_row_max(causal):
+    """As in the bf16 forward: masked keys (padding, or causal future keys of the diagonal
+    tile) with scores ~250 log2 units above every valid score must not move the row max."""
+    B, H, N, d = 2, 2, 640, 128
+    Q, K, _V = workloads.prefill_inputs(B, H, N, d, seed=93)
+    Qf = Q.float() * 0.5 + 1.0
+    Kf = K.float() * 0.5
+    key_len = None
+    if causal:
+        Kf[:, :, 127::128] = 16.0
+    else:
+        key_len = [400, 577]
+        for b, kl in enumerate(key_len):
+            Kf[b, :, kl:] = 16.0
+    Q8, K8, V8 = (t.to(torch.float8_e4m3fn) for t in (Qf, Kf, _V.float()))
+    O, L = _run(Q8, K8, V8, causal, key_len)
+    Oref, Lref = oracle.sdpa_forward_e4m3(Q8, K8, V8, causal=causal, key_len=key_len)
+    compare(f"fp8 masked huge keys c{int(causal)}", O, L, Oref, Lref)
+
+
 def test_fp8_forward_equals_bf16_forward_of_the_same_values():
     """E4M3 values are bf16 values: the FP8 path must match fa_forward on them (S differs only
     in fp32 summation order)."""

@@ -28,7 +28,10 @@
 //       O_t += P_t V_j         (A = P from TMEM, B = V from shared memory)
 //     and signals completion through tcgen05.commit -> mbarrier.
 //   * warps 4-7 / 8-11: softmax warpgroups for query tile 0 / 1, one thread
-//     per query row.  They read S from TMEM, mask, update (m, l), write
+//     per query row.  They read S from TMEM with tcgen05.ld.red, an sm_103a
+//     load that also returns each row's maximum over the loaded columns
+//     (tiles with masked entries reduce the masked row instead), mask,
+//     update (m, l), write
 //     P = bf16(exp2(S*scale*log2e - m)) over the first half of S's TMEM
 //     columns, and rescale O in TMEM by alpha when some row's max moved.
 //     At the end they normalise O by 1/l, stage it in shared memory in the

@@ -133,3 +133,85 @@ def test_f64_forward_equals_bf16_oracle_on_bf16_values():
         O2, L2 = oracle.sdpa_forward_f64(Q, K, V, causal=causal, key_len=kl)
         np.testing.assert_array_equal(O1, O2)
         np.testing.assert_array_equal(L1, L2)
+
+
+# ---------------------------------------------------------------------------
+# The magnitude arrays M_dV, M_dK, M_dQ set the per-element tolerance of every
+# GPU gradient comparison, so they are pinned on their own: to the gradient
+# they bound where that bound is attained exactly, to a closed form with one
+# valid key, and to a from-scratch 50-digit evaluation of their definition.
+# ---------------------------------------------------------------------------
+
+def test_magnitude_dV_equals_dV_of_absolute_upstream_gradient():
+    # dV_j = sum_i P_ij dO_i ("Blocked gradient computation": dV = P^T dO), and
+    # P >= 0, so with |dO| as the upstream gradient every term is nonnegative:
+    # the sum of term magnitudes for dO equals the gradient for |dO| exactly.
+    # That gradient is taken from torch.autograd in float64, not from the oracle.
+    B, H, N, d = 1, 2, 23, 6
+    g = torch.Generator().manual_seed(61)
+    Q, K, V, G = (torch.randn(B, H, N, d, generator=g, dtype=torch.float64) for _ in range(4))
+    for causal in (False, True):
+        v = V.clone().requires_grad_(True)
+        torch.nn.functional.scaled_dot_product_attention(Q, K, v, is_causal=causal).backward(G.abs())
+        m = oracle.sdpa_backward(Q, K, V, G, causal=causal, magnitudes=True)
+        np.testing.assert_allclose(m["M_dV"], v.grad.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_magnitudes_one_valid_key_closed_form():
+    # One valid key (key_len = 1): P_i0 = 1, O_i = V_0, dP_i0 = dO_i . V_0 and
+    # D_i = dP_i0.  So A_i = |D_i| + sum_c |dO_ic| |V_0c| and
+    #   M_dV[0]   = sum_i |dO_i|
+    #   M_dK[0,c] = scale sum_i (|dP_i0| + A_i) |Q_ic|
+    #   M_dQ[i,c] = scale (|dP_i0| + A_i) |K_0c|
+    # while every other key has all-zero magnitudes.
+    B, H, N, d = 1, 2, 6, 4
+    Q, K, V, G = (_rand((B, H, N, d), s) for s in (71, 72, 73, 74))
+    scale = 0.45
+    m = oracle.sdpa_backward(Q, K, V, G, scale=scale, key_len=[1], magnitudes=True)
+    for h in range(H):
+        q, k0, v0, g = Q[0, h], K[0, h, 0], V[0, h, 0], G[0, h]
+        dp = g @ v0                              # [N]
+        A = np.abs(dp) + np.abs(g) @ np.abs(v0)  # |D| = |dP| here
+        w = np.abs(dp) + A
+        np.testing.assert_allclose(m["M_dV"][0, h, 0], np.abs(g).sum(axis=0), rtol=1e-13)
+        np.testing.assert_allclose(m["M_dK"][0, h, 0], scale * (w[:, None] * np.abs(q)).sum(axis=0), rtol=1e-13)
+        np.testing.assert_allclose(m["M_dQ"][0, h], scale * w[:, None] * np.abs(k0)[None, :], rtol=1e-13)
+        for name in ("M_dV", "M_dK"):
+            assert np.all(m[name][0, h, 1:] == 0), name
+
+
+def test_magnitudes_match_50_digit_evaluation():
+    # Tiny inputs (N <= 7): every quantity the magnitudes are made of (scores,
+    # the softmax P, dP = dO V^T, D = rowsum(dO o O), O = P V) is recomputed in
+    # 50-digit arithmetic straight from the inputs, then the three sums.
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 50
+    B, H, N, d = 2, 1, 7, 3
+    Q, K, V, G = (_rand((B, H, N, d), s, amp=1.3) for s in (81, 82, 83, 84))
+    scale = 0.6
+    for causal, key_len in ((False, None), (True, None), (False, [5, 7])):
+        m = oracle.sdpa_backward(Q, K, V, G, causal=causal, scale=scale, key_len=key_len, magnitudes=True)
+        for b in range(B):
+            q, k, v, g = (X[b, 0] for X in (Q, K, V, G))
+            MdV = [[mp.mpf(0)] * d for _ in range(N)]
+            MdK = [[mp.mpf(0)] * d for _ in range(N)]
+            MdQ = [[mp.mpf(0)] * d for _ in range(N)]
+            for i in range(N):
+                keys = [j for j in range(N) if (key_len is None or j < key_len[b]) and (not causal or j <= i)]
+                s = {j: mp.mpf(scale) * mp.fsum(mp.mpf(q[i, c]) * mp.mpf(k[j, c]) for c in range(d)) for j in keys}
+                den = mp.fsum(mp.exp(x) for x in s.values())
+                P = {j: mp.exp(s[j]) / den for j in keys}
+                dP = {j: mp.fsum(mp.mpf(g[i, c]) * mp.mpf(v[j, c]) for c in range(d)) for j in keys}
+                O = [mp.fsum(P[j] * mp.mpf(v[j, c]) for j in keys) for c in range(d)]
+                D = mp.fsum(mp.mpf(g[i, c]) * O[c] for c in range(d))
+                A = abs(D) + mp.fsum(abs(mp.mpf(g[i, c])) * abs(O[c]) for c in range(d))
+                for j in keys:
+                    w = P[j] * (abs(dP[j]) + A)
+                    for c in range(d):
+                        MdV[j][c] += P[j] * abs(mp.mpf(g[i, c]))
+                        MdK[j][c] += mp.mpf(scale) * w * abs(mp.mpf(q[i, c]))
+                        MdQ[i][c] += mp.mpf(scale) * w * abs(mp.mpf(k[j, c]))
+            for name, M in (("M_dV", MdV), ("M_dK", MdK), ("M_dQ", MdQ)):
+                exact = np.array([[float(x) for x in row] for row in M])
+                np.testing.assert_allclose(m[name][b, 0], exact, rtol=1e-13, atol=1e-15,
+                                           err_msg=f"{name} causal={causal} key_len={key_len}")

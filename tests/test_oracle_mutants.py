@@ -47,6 +47,15 @@ MUTANTS = {
     "bwd_dK_no_scale": ("dKb[(size_t)j * d + c] += scale * ds * q[c];", "dKb[(size_t)j * d + c] += ds * q[c];"),
     "bwd_dQ_uses_values": ("dq[c] += scale * ds * kb[(size_t)j * d + c];",
                            "dq[c] += scale * ds * vb[(size_t)j * d + c];"),
+    # backward term magnitudes (the GPU gradient tolerance)
+    "bwd_MdV_inflated": ("MdV[(size_t)j * d + c] += pr[j] * fabs(g[c]);",
+                         "MdV[(size_t)j * d + c] += 64.0 * pr[j] * fabs(g[c]);"),
+    "bwd_MdK_inflated": ("MdK[(size_t)j * d + c] += scale * w * fabs(q[c]);",
+                         "MdK[(size_t)j * d + c] += 64.0 * scale * w * fabs(q[c]);"),
+    "bwd_MdQ_inflated": ("MdQ[(size_t)i * d + c] += scale * w * fabs(kb[(size_t)j * d + c]);",
+                         "MdQ[(size_t)i * d + c] += 64.0 * scale * w * fabs(kb[(size_t)j * d + c]);"),
+    "bwd_mag_drops_A": ("const double w = pr[j] * (fabs(dp[j]) + A);", "const double w = pr[j] * fabs(dp[j]);"),
+    "bwd_mag_A_drops_D": ("double A = fabs(D);", "double A = 0.0;"),
     # E4M3 decoding
     "e4m3_bias_off_by_one": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
     "e4m3_subnormal_scale": ("v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);"),

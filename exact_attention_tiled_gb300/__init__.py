@@ -19,7 +19,7 @@ import os
 import threading
 
 __all__ = ["fa_forward", "fa_forward_host", "fa_forward_host_workspace_bytes", "fa_forward_fp8", "fa_backward", "fa_backward_workspace_bytes", "fa_decode", "fa_decode_paged", "fa_decode_plan", "fa_decode_workspace_bytes",
-           "fa_device_error", "FaError", "library", "library_path", "STATUS"]
+           "fa_device_error", "fa_get_last_device_error", "FaError", "library", "library_path", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libfa.so")
@@ -79,14 +79,18 @@ def library():
         lib.fa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, ctypes.c_float,
                                           _i, _vp]
         lib.fa_decode_noalloc.restype = _i
-        lib.fa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _vp]
+        lib.fa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
         lib.fa_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_decode_workspace_bytes_for_lengths.argtypes = [_i, _i, _i, _i, _i, _vp]
+        lib.fa_decode_workspace_bytes_for_lengths.restype = ctypes.c_size_t
         lib.fa_decode_plan.argtypes = [_i, _i, _i, _i, _i, _vp, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]
         lib.fa_decode_plan.restype = _i
         lib.fa_status_string.argtypes = [_i]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_device_error.argtypes = [_i, ctypes.POINTER(_i)]
         lib.fa_device_error.restype = _i
+        lib.fa_get_last_device_error.argtypes = []
+        lib.fa_get_last_device_error.restype = _i
         lib.fa_version.restype = _i
         lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
         lib.fa_selftest_wait_timeout.restype = _i
@@ -314,8 +318,12 @@ def fa_decode_plan(B, H, Lmax, d, num_splits=0, seqlens_host=None, num_sms=0):
 
 
 def fa_decode_workspace_bytes(B, H, Lmax, d, num_splits=0, seqlens_host=None):
+    """Decode workspace bytes: without seqlens_host the bound for any lengths,
+    with it the exact size of that call on the current device."""
+    if seqlens_host is None:
+        return int(library().fa_decode_workspace_bytes(B, H, Lmax, d, num_splits))
     hp, keep = _host_i32(seqlens_host)
-    n = library().fa_decode_workspace_bytes(B, H, Lmax, d, num_splits, hp)
+    n = library().fa_decode_workspace_bytes_for_lengths(B, H, Lmax, d, num_splits, hp)
     del keep
     return int(n)
 
@@ -345,7 +353,7 @@ def fa_decode(q, Kcache, Vcache, seqlens, num_splits=0, scale=None, seqlens_host
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((B, H), device=q.device, dtype=torch.float32)
-    need = library().fa_decode_workspace_bytes(B, H, Lmax, d, num_splits, hp)
+    need = library().fa_decode_workspace_bytes_for_lengths(B, H, Lmax, d, num_splits, hp)
     if workspace is None:
         workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
     st = library().fa_decode(_ptr(q), _ptr(Kcache), _ptr(Vcache), _ptr(seqlens), hp, _ptr(out),
@@ -388,7 +396,7 @@ def fa_decode_paged(q, Kpool, Vpool, block_table, seqlens, num_splits=0, scale=N
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((B, H), device=q.device, dtype=torch.float32)
-    need = library().fa_decode_workspace_bytes(B, H, max_blocks * bs, d, num_splits, hp)
+    need = library().fa_decode_workspace_bytes_for_lengths(B, H, max_blocks * bs, d, num_splits, hp)
     if workspace is None:
         workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
     st = library().fa_decode_paged(_ptr(q), _ptr(Kpool), _ptr(Vpool), _ptr(block_table), max_blocks,
@@ -406,3 +414,8 @@ def fa_device_error(clear=True):
     site = _i()
     st = library().fa_device_error(int(bool(clear)), ctypes.byref(site))
     return st, site.value
+
+
+def fa_get_last_device_error():
+    """Status of the device error word, which is then reset; synchronises the device."""
+    return int(library().fa_get_last_device_error())

@@ -78,6 +78,14 @@ fa_status device_decode_ctas(int d, int *out) {
 
 int clamp_len(int v, int lmax) { return v < 0 ? 0 : (v > lmax ? lmax : v); }
 
+}  // namespace
+
+cudaError_t current_sm_count(int *out) {
+    return device_sm_count(out) == FA_OK ? cudaSuccess : cudaErrorInvalidDevice;
+}
+
+namespace {
+
 int round_up(long long v, int g) { return static_cast<int>((v + g - 1) / g * g); }
 
 // Split plan ("science-depth M4-055", trade-off 3: the chunk count is chosen
@@ -158,6 +166,20 @@ void plan_decode(int B, int H, int Lmax, int num_splits, const int32_t *seqlens_
     *smax = (max_len + c - 1) / c;
 }
 
+// The largest per-sequence chunk count plan_decode can return for sequences of
+// at most Lmax tokens, whatever the lengths and the SM count: a fixed count is
+// used as given; the automatic plans use chunks of >= 4 granules (one wave, or
+// mixed lengths), or of >= 1 granule with at most 1024 chunks (several waves of
+// equal lengths).
+int smax_bound(int Lmax, int num_splits) {
+    if (num_splits > 0) return num_splits;
+    const long long g1 = (static_cast<long long>(Lmax) + kDecodeGranule - 1) / kDecodeGranule;
+    const long long g4 = (static_cast<long long>(Lmax) + 4 * kDecodeGranule - 1) / (4 * kDecodeGranule);
+    long long s = g1 < 1024 ? g1 : 1024;
+    if (g4 > s) s = g4;
+    return static_cast<int>(s < 1 ? 1 : s);
+}
+
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 size_t workspace_for(int B, int H, int smax, int d) {
@@ -236,8 +258,8 @@ fa_status fa_decode_plan(int B, int H, int Lmax, int d, int num_splits, const in
     return FA_OK;
 }
 
-size_t fa_decode_workspace_bytes(int B, int H, int Lmax, int d, int num_splits,
-                                 const int32_t *seqlens_host) {
+size_t fa_decode_workspace_bytes_for_lengths(int B, int H, int Lmax, int d, int num_splits,
+                                             const int32_t *seqlens_host) {
     if (!decode_shape_ok(B, H, Lmax, d)) return 0;
     int chunk = 0, smax = 0;
     if (num_splits > 0) {
@@ -247,6 +269,13 @@ size_t fa_decode_workspace_bytes(int B, int H, int Lmax, int d, int num_splits,
     }
     return workspace_for(B, H, smax, d);
 }
+
+size_t fa_decode_workspace_bytes(int B, int H, int Lmax, int d, int num_splits) {
+    if (!decode_shape_ok(B, H, Lmax, d)) return 0;
+    return workspace_for(B, H, smax_bound(Lmax, num_splits), d);
+}
+
+fa_status fa_get_last_device_error(void) { return fa_device_error(1, nullptr); }
 
 }  // extern "C"
 
@@ -524,6 +553,10 @@ bool host_plan(int B, int H, int N, int d, int heads_per_group, HostPlan *pl) {
 struct HostStreams {
     cudaStream_t up, st[kHostSlots];
     cudaEvent_t start, h2d[kHostSlots], d2h[kHostSlots];
+    // Held by a call while it enqueues on these streams and records these
+    // events, so calls from several host threads on one device queue their
+    // work one after the other instead of interleaving event records.
+    std::mutex enqueue;
 };
 
 cudaError_t host_streams(HostStreams **out) {
@@ -578,6 +611,7 @@ fa_status fa_forward_host(const void *Qh, const void *Kh, const void *Vh, void *
     if (s != FA_OK) return s;
     HostStreams *hs = nullptr;
     if (host_streams(&hs) != cudaSuccess) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> serial(hs->enqueue);
     const cudaStream_t caller = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *kl_dev = key_len_host ? reinterpret_cast<int32_t *>(ws + pl.slots * pl.slot) : nullptr;

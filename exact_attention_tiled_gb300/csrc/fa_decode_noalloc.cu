@@ -48,7 +48,7 @@ extern "C" FA_API fa_status fa_decode_noalloc(const void *q, const void *Kcache,
                                               const int32_t *seqlens, const int32_t *seqlens_host, void *O,
                                               float *L, int B, int H, int Lmax, int d, float scale,
                                               int num_splits, fa_stream_t stream) {
-    const size_t need = fa_decode_workspace_bytes(B, H, Lmax, d, num_splits, seqlens_host);
+    const size_t need = fa_decode_workspace_bytes_for_lengths(B, H, Lmax, d, num_splits, seqlens_host);
     if (need == 0) {
         // arguments fa_decode rejects: let it report which one
         return fa_decode(q, Kcache, Vcache, seqlens, seqlens_host, O, L, B, H, Lmax, d, scale, num_splits,

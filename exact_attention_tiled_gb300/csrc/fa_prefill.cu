@@ -69,6 +69,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstring>
 
 #include "fa_internal.h"
@@ -848,27 +849,23 @@ cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     // setmaxnreg.inc only completes when the registers it asks for exist in
     // the block's launch allocation: refuse to launch a build where they do not.
-    static int regs_ok = -1;
-    if (regs_ok < 0) {
+    // (a property of the compiled kernel, the same on every device: computed once)
+    static std::atomic<int> regs_ok{-1};
+    if (regs_ok.load() < 0) {
         cudaFuncAttributes fa_attr;
         e = cudaFuncGetAttributes(&fa_attr, prefill_kernel<D, QK8>);
         if (e != cudaSuccess) return e;
         const long long have = static_cast<long long>(fa_attr.numRegs) * kThreads;
         const long long want = 2ll * 128 * kRegsSoftmax + 128ll * kRegsAux;
-        regs_ok = (have >= want && fa_attr.numRegs >= kRegsAux && fa_attr.numRegs <= kRegsSoftmax) ? 1 : 0;
+        regs_ok.store((have >= want && fa_attr.numRegs >= kRegsAux && fa_attr.numRegs <= kRegsSoftmax) ? 1 : 0);
     }
-    if (!regs_ok) return cudaErrorInvalidConfiguration;
+    if (!regs_ok.load()) return cudaErrorInvalidConfiguration;
     const int npairs = (p.N + 2 * BM - 1) / (2 * BM);
     const long long items = static_cast<long long>(npairs) * p.H * p.B;
     if (items > (1ll << 30)) return cudaErrorInvalidValue;
-    static int sms = 0;
-    if (!sms) {
-        int dev = 0;
-        e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
+    int sms = 0;
+    e = current_sm_count(&sms);
+    if (e != cudaSuccess) return e;
     // persistent: one CTA per SM (shared memory and TMEM allow no more)
     const int grid = static_cast<int>(items < sms ? items : sms);
     // (batch, head) units per L2 block.  Non-causal items all cost the same,

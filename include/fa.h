@@ -223,12 +223,24 @@ FA_API fa_status fa_decode(const void *q, const void *Kcache, const void *Vcache
                     void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
- * Workspace bytes fa_decode needs for these arguments (same meaning as
- * there; seqlens_host may be NULL).  Returns 0 for arguments fa_decode
- * would reject.
+ * Workspace bytes that suffice for every fa_decode call with these B, H,
+ * Lmax, d and num_splits, whatever the sequence lengths and seqlens_host
+ * (NULL included) and whatever the SM count: a buffer of this size can be
+ * allocated once and reused.  With num_splits > 0 it is exact; with automatic
+ * chunking it is the bound B * H * s_max * (d + 2) * 4 bytes (plus alignment),
+ * s_max = max(ceil(Lmax / 256), min(ceil(Lmax / 64), 1024)) chunks per
+ * sequence.  Returns 0 for arguments fa_decode would reject.
  */
-FA_API size_t fa_decode_workspace_bytes(int B, int H, int Lmax, int d, int num_splits,
-                                 const int32_t *seqlens_host);
+FA_API size_t fa_decode_workspace_bytes(int B, int H, int Lmax, int d, int num_splits);
+
+/*
+ * The exact workspace bytes of one fa_decode call on the current device:
+ * same arguments as there (seqlens_host may be NULL), never more than
+ * fa_decode_workspace_bytes(B, H, Lmax, d, num_splits).  Returns 0 for
+ * arguments fa_decode would reject.
+ */
+FA_API size_t fa_decode_workspace_bytes_for_lengths(int B, int H, int Lmax, int d, int num_splits,
+                                                    const int32_t *seqlens_host);
 
 /*
  * The split plan fa_decode would use: writes the chunk length in tokens and
@@ -254,11 +266,13 @@ FA_API fa_status fa_decode_plan(int B, int H, int Lmax, int d, int num_splits,
  * every GPU that loads it, until the process exits.  The call allocates
  * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  *
- *   - A request whose fa_decode_workspace_bytes() exceeds
+ *   - A request whose fa_decode_workspace_bytes_for_lengths() exceeds
  *     FA_DECODE_NOALLOC_MAX_BYTES returns FA_ERR_WORKSPACE and launches
  *     nothing; use fa_decode with your own workspace for it.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept for the life of the process: after a
+ *     cudaDeviceReset() it is stale, as is the device error word's.
  *   - Every call on a device uses the same array.  Nothing in it needs to
  *     start at zero (each partial is written before it is read), but two
  *     calls that overlap on the GPU, e.g. on two streams, race on it: order
@@ -292,9 +306,9 @@ FA_API fa_status fa_decode_noalloc(const void *q, const void *Kcache, const void
  *   num_blocks    pool size in blocks, >= 1.
  *   block_size    tokens per block, 1 .. FA_PAGED_MAX_BLOCK_SIZE.  Any value
  *                 is exact; a multiple of 16 keeps each copy >= 2 KB.
- *   O, L, d, scale, num_splits, workspace, stream: as in fa_decode; the
- *                 workspace size is fa_decode_workspace_bytes(B, H,
- *                 max_blocks * block_size, d, num_splits, seqlens_host).
+ *   O, L, d, scale, num_splits, workspace, stream: as in fa_decode, with
+ *                 Lmax = max_blocks * block_size in the workspace queries
+ *                 (fa_decode_workspace_bytes and ..._for_lengths).
  *
  * A table entry read on the device that lies outside [0, num_blocks) is
  * never dereferenced: block 0 is read in its place and the device error
@@ -324,6 +338,14 @@ FA_API const char *fa_status_string(fa_status s);
  * clear != 0 resets the word.
  */
 FA_API fa_status fa_device_error(int clear, int *site);
+
+/*
+ * fa_get_last_device_error -- the device error word of the current device,
+ * read and then reset, like cudaGetLastError: FA_OK, FA_ERR_DEVICE_TIMEOUT or
+ * FA_ERR_INVALID_ARG as in fa_device_error (which also reports the site and
+ * can leave the word set).  Synchronises the device.
+ */
+FA_API fa_status fa_get_last_device_error(void);
 
 /*
  * fa_selftest_wait_timeout -- exercise the bounded-wait failure path.

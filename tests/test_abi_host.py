@@ -29,8 +29,35 @@ def _declared_symbols():
 
 def test_header_declares_the_api():
     names = _declared_symbols()
-    assert {"fa_forward", "fa_decode", "fa_decode_workspace_bytes", "fa_decode_plan",
-            "fa_status_string", "fa_device_error", "fa_version"} <= set(names)
+    # the boundary's calls, by the names the scope table gives them
+    assert {"fa_forward", "fa_decode", "fa_decode_workspace_bytes", "fa_status_string",
+            "fa_get_last_device_error"} <= set(names)
+    # and this library's additions
+    assert {"fa_decode_plan", "fa_decode_workspace_bytes_for_lengths", "fa_device_error", "fa_version",
+            "fa_decode_paged", "fa_backward", "fa_forward_fp8", "fa_forward_host",
+            "fa_decode_noalloc"} <= set(names)
+
+
+def test_boundary_signatures(lib):
+    """Each boundary call, through ctypes, with the argument list the header gives it."""
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    flat = " ".join(text.split())
+    assert "size_t fa_decode_workspace_bytes(int B, int H, int Lmax, int d, int num_splits);" in flat
+    assert "fa_status fa_get_last_device_error(void);" in flat
+    assert ("fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *L, int B, int H, "
+            "int N, int d, int causal, float scale, const int32_t *key_len, fa_stream_t stream);") in flat
+    f = lib.fa_decode_workspace_bytes
+    f.argtypes = [ctypes.c_int] * 5
+    f.restype = ctypes.c_size_t
+    assert f(1, 32, 32768, 128, 8) > 0
+    assert f(1, 32, 32768, 96, 8) == 0
+    g = lib.fa_get_last_device_error
+    g.argtypes = []
+    g.restype = ctypes.c_int
+    # without a GPU the device cannot be queried: a CUDA error, never a crash
+    import torch
+    if not torch.cuda.is_available():
+        assert g() == 3
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -93,14 +120,42 @@ def test_decode_rejects_bad_arguments_before_cuda(lib):
     assert _dec(lib, ws=FAKE + 16) == 4        # workspace must be 256-byte aligned
 
 
+def _ws_bytes(B, H, smax, d):
+    up = lambda v: (v + 255) // 256 * 256
+    slots = B * H * smax
+    return up(slots * d * 4) + up(slots * 2 * 4)
+
+
 def test_workspace_bytes_fixed_splits(lib):
     B, H, Lmax, d, S = 3, 5, 1000, 128, 7
-    got = lib.fa_decode_workspace_bytes(B, H, Lmax, d, S, None)
-    slots = B * H * S
-    up = lambda v: (v + 255) // 256 * 256
-    assert got == up(slots * d * 4) + up(slots * 2 * 4)
-    assert lib.fa_decode_workspace_bytes(B, H, Lmax, 96, S, None) == 0
-    assert lib.fa_decode_workspace_bytes(0, H, Lmax, d, S, None) == 0
+    assert lib.fa_decode_workspace_bytes(B, H, Lmax, d, S) == _ws_bytes(B, H, S, d)
+    assert lib.fa_decode_workspace_bytes_for_lengths(B, H, Lmax, d, S, None) == _ws_bytes(B, H, S, d)
+    assert lib.fa_decode_workspace_bytes(B, H, Lmax, 96, S) == 0
+    assert lib.fa_decode_workspace_bytes(0, H, Lmax, d, S) == 0
+    assert lib.fa_decode_workspace_bytes_for_lengths(0, H, Lmax, d, S, None) == 0
+
+
+def test_workspace_bound_covers_every_automatic_plan(lib):
+    """The five-argument size is enough for the plan of any lengths on any SM count."""
+    import random
+    import exact_attention_tiled_gb300 as fa
+    rng = random.Random(7)
+    for _ in range(300):
+        B, H = rng.randint(1, 40), rng.choice([1, 2, 8, 32, 64])
+        Lmax = rng.choice([1, 63, 64, 65, 255, 257, 1000, 4096, 32768, 65536, 300000])
+        d = rng.choice([64, 128])
+        kind = rng.random()
+        if kind < 0.3:
+            lens = [Lmax] * B
+        elif kind < 0.5:
+            lens = [rng.randint(1, Lmax)] * B
+        else:
+            lens = [rng.randint(0, Lmax) for _ in range(B)]
+        bound = lib.fa_decode_workspace_bytes(B, H, Lmax, d, 0)
+        for sms in (1, 8, 152, 2000):
+            for hp in (lens, None):
+                _, smax = fa.fa_decode_plan(B, H, Lmax, d, 0, hp, sms)
+                assert _ws_bytes(B, H, smax, d) <= bound, (B, H, Lmax, d, sms, hp is None)
 
 
 def _plan(B, H, Lmax, d, splits, seqlens=None, sms=152):

@@ -29,6 +29,10 @@ def test_wait_that_runs_out_reports_timeout_and_context_survives():
     assert st == FA_ERR_DEVICE_TIMEOUT and site == SITE_SELFTEST
     st, site = fa.fa_device_error(clear=True)
     assert st == FA_OK
+    # the same through fa_get_last_device_error, which reads and resets the word
+    assert lib.fa_selftest_wait_timeout(2000, stream) == FA_OK
+    assert fa.fa_get_last_device_error() == FA_ERR_DEVICE_TIMEOUT
+    assert fa.fa_get_last_device_error() == FA_OK
     # the context still computes correctly
     Q, K, V = workloads.prefill_inputs(1, 2, 300, 64, seed=21)
     O, L = fa.fa_forward(Q.cuda(), K.cuda(), V.cuda(), causal=True)

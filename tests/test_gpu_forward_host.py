@@ -68,3 +68,38 @@ def test_host_forward_is_ordered_on_the_callers_stream():
     Od, Ld = _device_reference(Q, K, V, False, None)
     assert torch.equal(O.view(torch.int16), Od.view(torch.int16))
     assert torch.equal(L, Ld)
+
+
+def test_host_forward_from_two_host_threads():
+    # two host threads share the device's internal streams and events; each call
+    # enqueues its whole pipeline under the device's lock, so both results stay
+    # identical to fa_forward
+    import threading
+    cases = [workloads.prefill_inputs(2, 4, 384, 64, seed=51), workloads.prefill_inputs(1, 6, 640, 128, seed=52)]
+    cases = [tuple(t.pin_memory() for t in c) for c in cases]
+    refs = [_device_reference(*c, True, None) for c in cases]
+    results, errors = {}, []
+
+    def worker(i):
+        try:
+            s = torch.cuda.Stream()
+            outs = []
+            for _ in range(4):
+                O, L = fa.fa_forward_host(*cases[i], causal=True, heads_per_group=1, stream=s)
+                outs.append((O, L))
+            s.synchronize()
+            results[i] = outs
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join(timeout=120)
+    assert not errors, errors
+    for i, (Od, Ld) in enumerate(refs):
+        for O, L in results[i]:
+            assert torch.equal(O.view(torch.int16), Od.view(torch.int16))
+            assert torch.equal(L, Ld)
+    assert fa.fa_device_error() == (0, 0)

@@ -50,7 +50,7 @@ def _run_pair(B, H, Lmax, d, lens, splits, seed):
                                scale, splits, stream)
     assert st == 0, f"fa_decode_noalloc returned {st}"
 
-    need = lib.fa_decode_workspace_bytes(B, H, Lmax, d, splits, hp)
+    need = lib.fa_decode_workspace_bytes_for_lengths(B, H, Lmax, d, splits, hp)
     assert 0 < need <= NOALLOC_MAX_BYTES
     ws = torch.empty(need, device=dev, dtype=torch.uint8)
     O_ref = torch.empty_like(q)
@@ -72,12 +72,33 @@ def test_noalloc_matches_workspace_entry_point_twice():
     _run_pair(B=3, H=4, Lmax=1000, d=64, lens=[999, 64, 500], splits=5, seed=62)
 
 
+# d = 64 and 25 * 31 * 41 = 31775 partial slots: 31775 * 64 * 4 bytes of O_k plus
+# 31775 * 8 bytes of (m_k, l_k), each rounded up to 256 bytes, fill the array exactly.
+EDGE = dict(B=25, H=31, Lmax=41 * 64, d=64, splits=41)
+
+
+def test_noalloc_request_that_fills_the_array_exactly():
+    lib = _lib()
+    e = EDGE
+    assert lib.fa_decode_workspace_bytes_for_lengths(e["B"], e["H"], e["Lmax"], e["d"], e["splits"], None) \
+        == NOALLOC_MAX_BYTES
+    lens = np.random.default_rng(63).integers(1, e["Lmax"] + 1, e["B"]).tolist()
+    lens[0] = e["Lmax"]
+    _run_pair(B=e["B"], H=e["H"], Lmax=e["Lmax"], d=e["d"], lens=lens, splits=e["splits"], seed=63)
+
+
 def test_noalloc_rejects_requests_beyond_its_array():
     lib = _lib()
-    B, H, Lmax, d, splits = 64, 64, 65536, 128, 64
-    need = lib.fa_decode_workspace_bytes(B, H, Lmax, d, splits, None)
+    e = EDGE
+    # one more chunk per sequence than the exact fit; null pointers: the size
+    # check comes first, and fa_decode would reject null pointers before a launch
+    need = lib.fa_decode_workspace_bytes_for_lengths(e["B"], e["H"], e["Lmax"], e["d"], e["splits"] + 1, None)
     assert need > NOALLOC_MAX_BYTES
-    fake = ctypes.c_void_p(0x100000)
-    st = lib.fa_decode_noalloc(fake, fake, fake, fake, None, fake, None, B, H, Lmax, d, ctypes.c_float(0.0),
+    st = lib.fa_decode_noalloc(None, None, None, None, None, None, None, e["B"], e["H"], e["Lmax"], e["d"],
+                               ctypes.c_float(0.0), e["splits"] + 1, None)
+    assert st == FA_ERR_WORKSPACE
+    B, H, Lmax, d, splits = 64, 64, 65536, 128, 64
+    assert lib.fa_decode_workspace_bytes_for_lengths(B, H, Lmax, d, splits, None) > NOALLOC_MAX_BYTES
+    st = lib.fa_decode_noalloc(None, None, None, None, None, None, None, B, H, Lmax, d, ctypes.c_float(0.0),
                                splits, None)
     assert st == FA_ERR_WORKSPACE

@@ -55,6 +55,9 @@ def library():
         lib = ctypes.CDLL(_LIB_PATH)
         lib.fa_forward.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp]
         lib.fa_forward.restype = _i
+        lib.fa_forward_count_tiles.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp,
+                                               _vp, _vp]
+        lib.fa_forward_count_tiles.restype = _i
         lib.fa_forward_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _i,
                                         _vp, ctypes.c_size_t, _vp]
         lib.fa_forward_host.restype = _i
@@ -135,11 +138,14 @@ def _host_i32(x):
 
 
 def fa_forward(Q, K, V, causal=False, scale=None, key_len=None, out=None, lse=None,
-               return_lse=True, stream=None):
+               return_lse=True, stream=None, tile_counts=None):
     """Exact attention forward.  Q, K, V: CUDA bf16 [B, H, N, d]; returns (O, L).
 
     key_len: optional CUDA int32 [B] key-padding lengths.  L is float32
     [B, H, N] (None when return_lse=False and no `lse` buffer is given).
+    tile_counts: optional CUDA int32 [B, H, 2]; when given, the call goes
+    through fa_forward_count_tiles and the tensor receives the number of S
+    and P V tile products issued per (batch, head).
     """
     torch = _torch()
     for n, t in (("Q", Q), ("K", K), ("V", V)):
@@ -157,9 +163,19 @@ def fa_forward(Q, K, V, causal=False, scale=None, key_len=None, out=None, lse=No
         if key_len.dtype != torch.int32 or not key_len.is_cuda or key_len.numel() != B:
             raise TypeError("key_len must be a CUDA int32 tensor with B entries")
         key_len = key_len.contiguous()
+    sc = float(scale) if scale is not None else 0.0
+    if tile_counts is not None:
+        if (tile_counts.dtype != torch.int32 or not tile_counts.is_cuda or tuple(tile_counts.shape) != (B, H, 2)
+                or not tile_counts.is_contiguous()):
+            raise TypeError("tile_counts must be a contiguous CUDA int32 tensor [B, H, 2]")
+        st = library().fa_forward_count_tiles(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), _ptr(lse), B, H, N, d,
+                                              int(bool(causal)), sc, _ptr(key_len), _ptr(tile_counts),
+                                              _stream_handle(stream))
+        if st != 0:
+            raise FaError(st, "fa_forward_count_tiles")
+        return out, lse
     st = library().fa_forward(_ptr(Q), _ptr(K), _ptr(V), _ptr(out), _ptr(lse), B, H, N, d,
-                              int(bool(causal)), float(scale) if scale is not None else 0.0,
-                              _ptr(key_len), _stream_handle(stream))
+                              int(bool(causal)), sc, _ptr(key_len), _stream_handle(stream))
     if st != 0:
         raise FaError(st, "fa_forward")
     return out, lse

@@ -466,9 +466,13 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
     return FA_OK;
 }
 
-fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *L, int B, int H,
-                     int N, int d, int causal, float scale, const int32_t *key_len,
-                     fa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status forward_impl(const void *Q, const void *K, const void *V, void *O, float *L, int B, int H, int N, int d,
+                       int causal, float scale, const int32_t *key_len, unsigned *tile_count,
+                       cudaStream_t stream) {
     if (!Q || !K || !V || !O) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
@@ -498,8 +502,31 @@ fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float
     p.causal = causal;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = err;
-    if (launch_prefill(p, d, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    p.tile_count = tile_count;
+    if (tile_count &&
+        cudaMemsetAsync(tile_count, 0, static_cast<size_t>(B) * H * 2 * sizeof(unsigned), stream) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (launch_prefill(p, d, stream) != cudaSuccess) return FA_ERR_CUDA;
     return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_forward(const void *Q, const void *K, const void *V, void *O, float *L, int B, int H,
+                     int N, int d, int causal, float scale, const int32_t *key_len,
+                     fa_stream_t stream) {
+    return forward_impl(Q, K, V, O, L, B, H, N, d, causal, scale, key_len, nullptr,
+                        static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_forward_count_tiles(const void *Q, const void *K, const void *V, void *O, float *L, int B, int H,
+                                 int N, int d, int causal, float scale, const int32_t *key_len,
+                                 unsigned *tile_counts, fa_stream_t stream) {
+    if (!tile_counts || !aligned(tile_counts, 4)) return FA_ERR_INVALID_ARG;
+    return forward_impl(Q, K, V, O, L, B, H, N, d, causal, scale, key_len, tile_counts,
+                        static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -49,6 +49,7 @@ struct PrefillParams {
     float scale_log2;       // scale * log2(e)
     unsigned *err;
     int qk_e4m3;            // Q and K are E4M3 [B, H, N, d] (d = 128); V stays bf16
+    unsigned *tile_count;   // nullptr, or device [B * H][2]: S and P V tile products issued
 };
 
 cudaError_t launch_prefill(const PrefillParams &p, int d, cudaStream_t stream);

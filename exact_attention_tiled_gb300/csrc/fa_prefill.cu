@@ -208,7 +208,10 @@ __device__ __forceinline__ int item_of_round(int r, int G, int c) {
     return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
-template <int D, bool QK8 = false>
+// kCount: the counting instantiation of fa_forward_count_tiles, which adds per
+// (batch, head) the tile products it issues to p.tile_count; the kernels of the
+// other entry points are compiled without it.
+template <int D, bool QK8 = false, bool kCount = false>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ TmapSet tm, const PrefillParams p, int num_items, int npairs, int upb) {
     using C = Cfg<D>;
@@ -397,6 +400,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr uint32_t idesc_o = idesc_bf16_f32(BM, D, 0, 1);
                 // A descriptor advanced by a byte offset: the start-address
                 // field holds address >> 4 and never carries (SMEM < 256 KB).
+                // per (batch, head): the S and the P V tile products issued
+                auto count = [&](int bh, int which) {
+                    if constexpr (kCount) {
+                        if (lane == 0) atomicAdd(p.tile_count + 2 * bh + which, 1u);
+                    }
+                };
                 auto issue_s = [&](int t, uint32_t kslot) {
                     const uint64_t qd = sdesc_sw128(q_smem + t * C::kTileBytes, 16, 1024);
                     const uint64_t kd = sdesc_sw128(kslot, 16, 1024);
@@ -447,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int t = 0; t < 2; ++t)
                             if (it.nkv[t] > 0) {
                                 issue_s(t, ring + (g % C::kSlots) * C::kTileBytes);
+                                count(it.bh, 0);
                                 mma_commit_warp(bar_s_full(t));
                             }
                         if (it.ntot == 1) mma_commit_warp(bar_q_free);  // the item's last S MMA is issued
@@ -476,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         }
                                         tc_fence_after();
                                         issue_s(t, kslot);
+                                        count(it.bh, 0);
                                         mma_commit_warp(bar_s_full(t));
                                     }
                                 }
@@ -497,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     ++pcnt[t];
                                     tc_fence_after();
                                     issue_pv(t, vslot, j);
+                                    count(it.bh, 1);
                                     // the item's last PV_t is announced by o_final, the others by pv_done
                                     mma_commit_warp(j + 1 == it.nkv[t] ? bar_o_final(t) : bar_pv_done(t));
                                 }
@@ -519,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 ++pcnt[t];
                                 tc_fence_after();
                                 issue_pv(t, vslot, j);
+                                count(it.bh, 1);
                                 if (j + 1 == it.nkv[t]) mma_commit_warp(bar_o_final(t));
                             }
                             if (j + 1 < it.nkv[t]) {
@@ -530,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     k_ready = true;
                                 }
                                 issue_s(t, kslot);
+                                count(it.bh, 0);
                                 mma_commit_warp(bar_s_full(t));
                             }
                         }
@@ -836,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
-template <int D, bool QK8 = false>
+template <int D, bool QK8 = false, bool kCount = false>
 cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
     TmapSet tm;
     std::memset(&tm, 0, sizeof tm);
@@ -845,7 +859,8 @@ cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
                           : make_map(&tm.q, p.Q, BH, p.N, D) && make_map(&tm.k, p.K, BH, p.N, D);
     if (!maps || !make_map(&tm.v, p.V, BH, p.N, D) || !make_map(&tm.o, p.O, BH, p.N, D)) return cudaErrorInvalidValue;
     const int smem = Cfg<D>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, QK8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_kernel<D, QK8, kCount>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // setmaxnreg.inc only completes when the registers it asks for exist in
     // the block's launch allocation: refuse to launch a build where they do not.
@@ -853,7 +868,7 @@ cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
     static std::atomic<int> regs_ok{-1};
     if (regs_ok.load() < 0) {
         cudaFuncAttributes fa_attr;
-        e = cudaFuncGetAttributes(&fa_attr, prefill_kernel<D, QK8>);
+        e = cudaFuncGetAttributes(&fa_attr, prefill_kernel<D, QK8, kCount>);
         if (e != cudaSuccess) return e;
         const long long have = static_cast<long long>(fa_attr.numRegs) * kThreads;
         const long long want = 2ll * 128 * kRegsSoftmax + 128ll * kRegsAux;
@@ -878,7 +893,7 @@ cudaError_t launch_d(const PrefillParams &p, cudaStream_t stream) {
     long long upb = p.causal ? BH : kL2BlockBytes / (kv_unit > 0 ? kv_unit : 1);
     if (upb < 1) upb = 1;
     if (upb > static_cast<long long>(BH)) upb = BH;
-    prefill_kernel<D, QK8><<<grid, kThreads, smem, stream>>>(tm, p, static_cast<int>(items), npairs,
+    prefill_kernel<D, QK8, kCount><<<grid, kThreads, smem, stream>>>(tm, p, static_cast<int>(items), npairs,
                                                               static_cast<int>(upb));
     return cudaGetLastError();
 }
@@ -916,7 +931,8 @@ cudaError_t launch_e4m3_to_bf16(const void *src, void *dst, long long n, cudaStr
 }
 
 cudaError_t launch_prefill(const PrefillParams &p, int d, cudaStream_t stream) {
-    if (p.qk_e4m3) return d == 128 ? launch_d<128, true>(p, stream) : cudaErrorInvalidValue;
+    if (p.qk_e4m3) return d == 128 && !p.tile_count ? launch_d<128, true>(p, stream) : cudaErrorInvalidValue;
+    if (p.tile_count) return d == 128 ? launch_d<128, false, true>(p, stream) : launch_d<64, false, true>(p, stream);
     return d == 128 ? launch_d<128>(p, stream) : launch_d<64>(p, stream);
 }
 

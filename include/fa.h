@@ -93,6 +93,24 @@ FA_API fa_status fa_forward(const void *Q, const void *K, const void *V, void *O
                      const int32_t *key_len, fa_stream_t stream);
 
 /*
+ * fa_forward_count_tiles -- fa_forward that also counts, per (batch, head),
+ * the 128 x 128 tile products the kernel issues: tile_counts[2 * (b * H + h)]
+ * the S = Q K^T products and tile_counts[2 * (b * H + h) + 1] the P V
+ * products.  It makes the causal tile skipping of "Infra: Flash Attention"
+ * (section "Symbols and boundary conditions", the causal figure) and "CMU
+ * 10-423 Lecture 18" (section 4.3, exercise 4: T(T+1)/2 of T^2 tiles)
+ * observable; the outputs are those of fa_forward.
+ *
+ *   tile_counts  DEVICE uint32 [B * H * 2], 4-byte aligned, zero-filled by
+ *                the call (on `stream`) before the kernel adds to it.
+ * Other arguments, results and errors: as in fa_forward.  The counting adds
+ * one atomic per tile product, so this call is for checking, not timing.
+ */
+FA_API fa_status fa_forward_count_tiles(const void *Q, const void *K, const void *V, void *O, float *L,
+                                        int B, int H, int N, int d, int causal, float scale,
+                                        const int32_t *key_len, unsigned *tile_counts, fa_stream_t stream);
+
+/*
  * fa_forward_host -- fa_forward over HOST buffers, with the host<->device
  * copies inside the call.  The (batch, head) slices are independent problems
  * ("Infra: Flash Attention", "Attention and its scope": each head attends on

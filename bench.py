@@ -48,6 +48,14 @@ def decode_bytes(H, lens, d):
     return float(sum(2 * H * n * d * 2 for n in lens))
 
 
+def spread(ms):
+    """Mean, median, extremes and standard deviation of per-step times (ms)."""
+    ms = list(ms)
+    return {"mean": round(statistics.mean(ms), 4), "median": round(statistics.median(ms), 4),
+            "min": round(min(ms), 4), "max": round(max(ms), 4),
+            "stdev": round(statistics.stdev(ms), 4) if len(ms) > 1 else 0.0, "n": len(ms)}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -425,6 +433,7 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(pf, 4),
+        "step_ms": spread(pf_ms),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -440,11 +449,12 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": recorded_traffic("prefill_kernel"),
                      "kernel": "prefill_kernel<128>"},
         "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(ee, 4),
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(ee, 4), "step_ms": spread(e2e_ms),
                 "path": "fa_forward_host: pinned host Q,K,V -> device by groups of heads, each group's "
                         "forward and O, L copy back overlapping the next groups' copies"},
         "decode": {"workload": DECODE, "value": round(gbs, 1), "unit": "GB/s",
-                   "ms_per_step": round(dc, 4), "bytes_per_step": dbytes, "num_splits": "auto",
+                   "ms_per_step": round(dc, 4), "step_ms": spread(dc_ms), "bytes_per_step": dbytes,
+                   "num_splits": "auto",
                    "chunk_len": chunk, "chunks_per_seq": nchunk, "gbs_by_num_splits": sweep,
                    "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1),
                                 "peak": peaks["hbm_gbs"], "unit": "GB/s",

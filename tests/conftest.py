@@ -28,3 +28,16 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _device_error_word_stays_clear(request):
+    """Every GPU test leaves the library's device error word clear: a bounded
+    wait that ran out inside a kernel (or invalid device data) fails the test
+    that caused it, even when that test's outputs happened to be right."""
+    yield
+    if request.node.get_closest_marker("gpu") is None or not has_gpu():
+        return
+    import exact_attention_tiled_gb300 as fa
+    st, site = fa.fa_device_error(clear=True)
+    assert st == 0, f"device error word set during {request.node.name}: status {st}, site {site:#x}"

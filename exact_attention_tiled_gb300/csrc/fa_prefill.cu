@@ -392,7 +392,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the lookahead schedule warp 1 issues the S products and warp 2
             // the P V products; otherwise warp 1 issues both.
             const bool do_s = !kLA || warp == kMmaWarp;
-            const bool do_pv = !kLA || warp == kPvWarp;
             bool issued_any = false;
             {
                 constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0, 0);

@@ -98,7 +98,7 @@ def load_peaks():
 KERNEL_SOURCES = {
     "prefill_kernel": ("fa_prefill.cu", "fa_ptx.cuh", "fa_internal.h", "fa_tmap.h"),
     "decode_split_kernel": ("fa_decode.cu", "fa_ptx.cuh", "fa_internal.h"),
-    "bwd_dkdv_kernel": ("fa_backward.cu", "fa_ptx.cuh", "fa_internal.h", "fa_tmap.h"),
+    "bwd_main_kernel": ("fa_backward.cu", "fa_ptx.cuh", "fa_internal.h", "fa_tmap.h"),
 }
 
 
@@ -413,7 +413,7 @@ def run_ours(args, rank, world, local_rank):
         fl = 2.5 * prefill_flops(B_, H_, N_, d_, causal_)
         others[name] = {"ms": round(ms, 4), "flops": fl, "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
                         "frac_of_bf16_peak": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                        "kernels": "bwd_pre + bwd_dkdv + bwd_dq (S and dP recomputed in both)"}
+                        "kernels": "bwd_pre + bwd_main (dK/dV and dQ CTAs in one grid; S and dP recomputed in both)"}
         del Qb, Kb, Vb, dOb, Ob, Lb, dQb, dKb, dVb
     st, site = fa.fa_device_error(clear=True)
     if st != 0:

@@ -10,9 +10,12 @@
 //   dS_ij = P_ij (dP_ij - D_i)
 //   dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K
 //
-// Three kernels, no N x N matrix in global memory:
+// Two kernels, no N x N matrix in global memory:
 //   * bwd_pre_kernel: D = rowsum(dO o O) in fp32 (bandwidth bound).
-//   * bwd_dkdv_kernel: one CTA per 128-key tile j of one (b, h).  K_j and V_j
+//   * bwd_main_kernel: one grid of two kinds of CTA, which need only D and
+//     so run side by side (the dQ CTAs fill the SMs the dK/dV CTAs leave idle
+//     in their last wave):
+//   * dK/dV CTAs: one per 128-key tile j of one (b, h).  K_j and V_j
 //     stay in shared memory; the query tiles i stream through a ring together
 //     with their dO_i, L_i and D_i.  Per half of a query tile (64 queries) the
 //     tensor core forms S^T = K_j Q_i^T and dP^T = V_j dO_i^T in TMEM (keys on
@@ -22,12 +25,12 @@
 //     dK += dS^T Q_i in TMEM with A read straight from TMEM.  Each half has its
 //     own TMEM buffer, so one half's exponentials overlap the other half's
 //     products.  dV, dK leave once, at the end.
-//   * bwd_dq_kernel: one CTA per 128-query tile i, the same half-step scheme
+//   * dQ CTAs: one per 128-query tile i, the same half-step scheme
 //     over key tiles: S = Q_i K_j^T and dP = dO_i V_j^T, dS in the compute
 //     warpgroups, and dQ += dS K_j in TMEM.  Computing dQ in its own pass
 //     (recomputing S and dP) keeps every gradient element written by exactly
 //     one CTA: no atomics, and the result does not depend on scheduling.
-// Warp roles in both main kernels (640 threads): warp 0 lane 0 issues the
+// Warp roles in both kinds of CTA (640 threads): warp 0 lane 0 issues the
 // TMA copies, warp 1 is the MMA warp (converged, one elected lane issues),
 // warps 4-19 are four compute warpgroups, one thread per TMEM lane (tile row).
 #include <cuda.h>
@@ -150,15 +153,15 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *O, co
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (row < rows && part == 0) Dout[row] = acc;
+    grid_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
-// dK, dV: grid (B*H, ceil(N/128)); blockIdx.y = key tile (heaviest first
-// under causal masking: key tile j meets the query tiles i >= j).
+// dK, dV of key tile jt of (batch, head) bh: one CTA (key tile 0 is the
+// heaviest under causal masking: key tile j meets the query tiles i >= j).
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_dkdv_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
+__device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, const int bh, const int jt) {
     using C = BwdCfg<D, HalfStepShape<D>::kStages>;
     constexpr int NB = HalfStepShape<D>::kHalfBufs;
     constexpr uint32_t kColGrad = HalfStepShape<D>::kColAccum;
@@ -187,7 +190,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x, jt = blockIdx.y;
     const int b = bh / p.H;
     const int N = p.N;
     const int T = (N + BT - 1) / BT;
@@ -238,6 +240,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tma_load_3d(v_smem + cb * (BT * 128), &tm.v, cb * 64, key0, bh, bar_kv, pol);
                 }
             }
+            // D comes from bwd_pre_kernel, which this grid may overlap (programmatic
+            // dependent launch): wait for it before the first read
+            grid_dependency_wait();
             for (int n = 0; n < nsteps && ok; ++n) {
                 const int s = n % C::kStages;
                 const int i = i_lo + n;
@@ -495,12 +500,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// dQ: grid (B*H, ceil(N/128)); blockIdx.y = query tile rank, heaviest first
-// under causal masking (query tile i meets the key tiles j <= i).
+// dQ of query tile rank `rank` of (batch, head) bh: one CTA; rank 0 is the
+// last query tile, the heaviest under causal masking (query tile i meets the
+// key tiles j <= i).
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_dq_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
+__device__ __forceinline__ void dq_cta(const BwdMaps &tm, const BwdParams &p, const int bh, const int rank) {
     using C = BwdCfg<D, HalfStepShape<D>::kStages>;
     constexpr int NB = HalfStepShape<D>::kHalfBufs;
     constexpr uint32_t kColGrad = HalfStepShape<D>::kColAccum;
@@ -531,11 +536,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
     const int b = bh / p.H;
     const int N = p.N;
     const int T = (N + BT - 1) / BT;
-    const int it = T - 1 - static_cast<int>(blockIdx.y);
+    const int it = T - 1 - rank;
     const int q0 = it * BT;
     int klen = N;
     if (p.key_len) klen = clampi(p.key_len[b], 0, N);
@@ -670,6 +674,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const float sl2 = p.scale_log2;
         float lrow = 0.f, drow = 0.f;
+        grid_dependency_wait();   // D of bwd_pre_kernel (programmatic dependent launch)
         if (q < N) {
             lrow = p.L[static_cast<size_t>(bh) * N + q] * kLog2e;
             drow = p.Dvec[static_cast<size_t>(bh) * N + q];
@@ -791,6 +796,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == kMma) tmem_dealloc(tmem, 512);
 }
 
+// dK/dV and dQ in one grid (B*H, 2 ceil(N/128)): rows y < T of the grid are
+// dK/dV CTAs, the others dQ CTAs.  The two halves are independent (both need
+// only D), so dQ CTAs fill the SMs that the dK/dV half leaves idle in its last
+// wave instead of waiting for a second launch.
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_main_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
+    const int T = (p.N + BT - 1) / BT;
+    const int y = static_cast<int>(blockIdx.y);
+    if (y < T)
+        dkdv_cta<D>(tm, p, static_cast<int>(blockIdx.x), y);
+    else
+        dq_cta<D>(tm, p, static_cast<int>(blockIdx.x), y - T);
+}
+
 template <int D>
 cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     const long long rows = static_cast<long long>(p.B) * p.H * p.N;
@@ -813,17 +833,23 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
         !make_map(&tm.dv, p.dV, BH, p.N, D))
         return cudaErrorInvalidValue;
     const int smem = BwdCfg<D, HalfStepShape<D>::kStages>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int T = (p.N + BT - 1) / BT;
-    const dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>(T));
-    bwd_dkdv_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tm, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    bwd_dq_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tm, p);
-    return cudaGetLastError();
+    if (2ll * T > 65535) return cudaErrorInvalidValue;
+    // launched as a programmatic dependent of bwd_pre_kernel: its CTAs set up
+    // (barriers, TMEM, the first K/V or Q/dO loads) while D is still being written
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(BH), static_cast<unsigned>(2 * T), 1);
+    cfg.blockDim = dim3(kBwdThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<D>, tm, p);
 }
 
 }  // namespace

@@ -70,9 +70,13 @@ def test_decode_variable_length_batch_sampled():
     L = L.cpu().numpy()
     assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
     lens = seqlens.tolist()
+    # the longest and the shortest sequence, every sequence at least once (each has its own
+    # chunk count), and seeded (b, h) pairs up to 64 of the 512
     picks = {(int(np.argmax(lens)), 0), (int(np.argmin(lens)), 31)}
     rng = np.random.default_rng(5)
-    while len(picks) < 24:
+    for b in range(len(lens)):
+        picks.add((b, int(rng.integers(32))))
+    while len(picks) < 64:
         picks.add((int(rng.integers(16)), int(rng.integers(32))))
     for b, h in sorted(picks):
         n = lens[b]

@@ -77,8 +77,15 @@ def _sampled(name, nrows, seed, use_key_len=True):
     assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
     B, H, N, d = Q.shape
     rows = workloads.sample_indices(B * H * N, nrows, seed).numpy()
-    # include tile boundaries of the first head
-    rows = np.unique(np.concatenate([rows, [127, 128, 255, 256, N - 128, N - 1]]))
+    # plus the rows at 128-row tile edges (and at the edges of 256-row work items) of the
+    # first, a middle and the last (batch, head) unit and of three more seeded ones; under
+    # causal masking the items holding rows 0..255 are the lightest, dealt in the last round
+    units = {0, (B * H) // 2, B * H - 1}
+    units.update(int(u) for u in workloads.sample_indices(B * H, 3, seed + 1).numpy())
+    edges = [r for r in (0, 1, 127, 128, 129, 255, 256, 511, 512, N - 257, N - 256, N - 129, N - 128, N - 1)
+             if 0 <= r < N]
+    extra = [u * N + r for u in sorted(units) for r in edges]
+    rows = np.unique(np.concatenate([rows, np.asarray(extra, dtype=rows.dtype)]))
     Oref, Lref = oracle.sdpa_rows(Q, K, V, rows, causal=causal, key_len=kl)
     compare(name, O.reshape(-1, d)[rows], L.reshape(-1)[rows], Oref, Lref)
 

@@ -16,7 +16,8 @@
 //     so run side by side (the dQ CTAs fill the SMs the dK/dV CTAs leave idle
 //     in their last wave):
 //   * dK/dV CTAs: one per 128-key tile j of one (b, h).  K_j and V_j
-//     stay in shared memory; the query tiles i stream through a ring together
+//     stay in shared memory (at d = 64 also in TMEM, the A operands of the
+//     S^T and dP^T products); the query tiles i stream through a ring together
 //     with their dO_i, L_i and D_i.  Per half of a query tile (64 queries) the
 //     tensor core forms S^T = K_j Q_i^T and dP^T = V_j dO_i^T in TMEM (keys on
 //     the 128 TMEM lanes, queries on the columns); two compute warpgroups turn
@@ -119,7 +120,8 @@ struct BwdCfg {
 // Both main kernels run a step (one 128-row tile of the streamed operand) as two
 // half-steps of 64 columns.  TMEM holds kHalfBufs half-step buffers of 128
 // columns (S half, then dP half) and then the accumulators; at d = 64 there is
-// room for three buffers, at d = 128 for two.  The streamed ring has one stage
+// room for three buffers, at d = 128 for two (the dK/dV kernel trades the
+// third for K_j and V_j, see dkdv_cta).  The streamed ring has one stage
 // more at d = 64 (shared memory allows it), so the deeper lookahead does not
 // wait on its loads.
 template <int D>
@@ -163,8 +165,16 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *O, co
 template <int D>
 __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, const int bh, const int jt) {
     using C = BwdCfg<D, HalfStepShape<D>::kStages>;
-    constexpr int NB = HalfStepShape<D>::kHalfBufs;
-    constexpr uint32_t kColGrad = HalfStepShape<D>::kColAccum;
+    // At d = 64 this kernel keeps two half-step buffers and copies K_j and V_j into
+    // TMEM (packed bf16 rows, one key per lane), so S^T = K Q_h^T and dP^T = V dO_h^T
+    // are TS products that read only Q_h and dO_h from shared memory (measured: d = 64
+    // backward +0.7 % against three buffers and SS products).  At d = 128 the
+    // accumulators leave no room: both operands come from shared memory.
+    constexpr bool kKvTmem = D == 64;
+    constexpr int NB = kKvTmem ? 2 : HalfStepShape<D>::kHalfBufs;
+    constexpr uint32_t kColGrad = 128u * NB;
+    constexpr uint32_t kColK = kColGrad + 2 * D, kColV = kColK + D / 2;
+    static_assert(!kKvTmem || kColV + D / 2 <= 512, "TMEM columns");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -185,7 +195,8 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
     auto bar_st = [&](int bf) { return bars + 8u * (1 + 2 * C::kStages + bf); };
     auto bar_ps = [&](int bf) { return bars + 8u * (1 + 2 * C::kStages + NB + bf); };
     const uint32_t bar_done = bars + 8u * (1 + 2 * C::kStages + 2 * NB);
-    static_assert(1 + 2 * C::kStages + 2 * NB + 1 <= C::kNumBars, "barrier slots");
+    const uint32_t bar_ktm = bar_done + 8u;   // K_j, V_j are in TMEM
+    static_assert(1 + 2 * C::kStages + 2 * NB + 2 <= C::kNumBars, "barrier slots");
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
@@ -211,6 +222,7 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
             mbar_init(bar_ps(bf), 8);
         }
         mbar_init(bar_done, 1);
+        mbar_init(bar_ktm, 8);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -292,7 +304,7 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
             constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT / 2, 0, 0);   // M 128 keys, N 64 queries
             constexpr uint32_t idesc_g = idesc_bf16_f32(BT, D, 0, 1);
             const int nhalf = 2 * nsteps;
-            bool ok = wait_abort_warp(bar_kv, 0, p.err, kSiteBwKV, abort_flag);
+            bool ok = wait_abort_warp(kKvTmem ? bar_ktm : bar_kv, 0, p.err, kSiteBwKV, abort_flag);
             const uint64_t kd = sdesc_sw128(k_smem, 16, 1024), vd = sdesc_sw128(v_smem, 16, 1024);
             // S^T = K Q_h^T and dP^T = V dO_h^T into buffer u % NB (K-major A and B; the
             // half's 64 query rows start 8 swizzle atoms into each column block).  The
@@ -311,12 +323,18 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                    mma_ss_warp(tmem + col, kd + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
+                    if (kKvTmem)
+                        mma_ts_warp(tmem + col, tmem + kColK + kk * 8, qd + off, idesc_s, kk > 0 ? 1u : 0u);
+                    else
+                        mma_ss_warp(tmem + col, kd + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                    mma_ss_warp(tmem + col + 64, vd + off, od + off, idesc_s, kk > 0 ? 1u : 0u);
+                    if (kKvTmem)
+                        mma_ts_warp(tmem + col + 64, tmem + kColV + kk * 8, od + off, idesc_s, kk > 0 ? 1u : 0u);
+                    else
+                        mma_ss_warp(tmem + col + 64, vd + off, od + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 mma_commit_warp(bar_st(u % NB));
                 return true;
@@ -372,6 +390,32 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
         bool ok = true;
         const int hf = h >> 1;   // the half of every step this warpgroup serves
         const int w = h & 1;     // its 32 columns within the half
+        if (kKvTmem && h < 2 && nsteps > 0) {
+            // warpgroup 0 copies this thread's row of K_j, warpgroup 1 its row of V_j,
+            // from the swizzled shared tile into TMEM as packed bf16 pairs
+            ok = wait_abort_warp(bar_kv, 0, p.err, kSiteBwKV, abort_flag);
+            if (ok) {
+                const uint8_t *tile = smem + C::kFixedOff + h * C::kTileBytes;
+#pragma unroll
+                for (int cb = 0; cb < D / 64; ++cb) {
+                    const uint8_t *row = tile + cb * (BT * 128) + r * 128;
+                    uint32_t wv[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(row + ((c ^ (r & 7)) << 4));
+                        wv[4 * c] = v.x;
+                        wv[4 * c + 1] = v.y;
+                        wv[4 * c + 2] = v.z;
+                        wv[4 * c + 3] = v.w;
+                    }
+                    tmem_st32(tmem + lane_off + (h ? kColV : kColK) + cb * 32, wv);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_ktm);
+        }
         for (int n = 0; n < nsteps && ok; ++n) {
             const int s = n % C::kStages;
             const int q0 = (i_lo + n) * BT;

@@ -99,6 +99,29 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// Row r of a 128-row bf16 tile held in shared memory in the tensor maps' 128-byte
+// swizzled layout (16-byte chunk c of row r at c ^ (r & 7)) into this thread's TMEM
+// lane as packed bf16 pairs, D / 2 columns from taddr: the row becomes the A operand
+// of TS products.  Called by one full warpgroup, thread r of the tile on lane r.
+template <int D>
+__device__ __forceinline__ void tile_row_to_tmem(const uint8_t *tile, int r, uint32_t taddr) {
+#pragma unroll
+    for (int cb = 0; cb < D / 64; ++cb) {
+        const uint8_t *row = tile + cb * (BT * 128) + r * 128;
+        uint32_t wv[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(row + ((c ^ (r & 7)) << 4));
+            wv[4 * c] = v.x;
+            wv[4 * c + 1] = v.y;
+            wv[4 * c + 2] = v.z;
+            wv[4 * c + 3] = v.w;
+        }
+        tmem_st32(taddr + cb * 32, wv);
+    }
+    tmem_wait_st();
+}
+
 template <int D, int Stages = 2>
 struct BwdCfg {
     static constexpr int kColBlocks = D / 64;
@@ -323,7 +346,7 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                    if (kKvTmem)
+                    if constexpr (kKvTmem)
                         mma_ts_warp(tmem + col, tmem + kColK + kk * 8, qd + off, idesc_s, kk > 0 ? 1u : 0u);
                     else
                         mma_ss_warp(tmem + col, kd + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
@@ -331,7 +354,7 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * (BT * 128) + (kk & 3) * 32) >> 4;
-                    if (kKvTmem)
+                    if constexpr (kKvTmem)
                         mma_ts_warp(tmem + col + 64, tmem + kColV + kk * 8, od + off, idesc_s, kk > 0 ? 1u : 0u);
                     else
                         mma_ss_warp(tmem + col + 64, vd + off, od + off, idesc_s, kk > 0 ? 1u : 0u);
@@ -394,24 +417,8 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
             // warpgroup 0 copies this thread's row of K_j, warpgroup 1 its row of V_j,
             // from the swizzled shared tile into TMEM as packed bf16 pairs
             ok = wait_abort_warp(bar_kv, 0, p.err, kSiteBwKV, abort_flag);
-            if (ok) {
-                const uint8_t *tile = smem + C::kFixedOff + h * C::kTileBytes;
-#pragma unroll
-                for (int cb = 0; cb < D / 64; ++cb) {
-                    const uint8_t *row = tile + cb * (BT * 128) + r * 128;
-                    uint32_t wv[32];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(row + ((c ^ (r & 7)) << 4));
-                        wv[4 * c] = v.x;
-                        wv[4 * c + 1] = v.y;
-                        wv[4 * c + 2] = v.z;
-                        wv[4 * c + 3] = v.w;
-                    }
-                    tmem_st32(tmem + lane_off + (h ? kColV : kColK) + cb * 32, wv);
-                }
-                tmem_wait_st();
-            }
+            if (ok)
+                tile_row_to_tmem<D>(smem + C::kFixedOff + h * C::kTileBytes, r, tmem + lane_off + (h ? kColV : kColK));
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_ktm);
@@ -731,24 +738,8 @@ __device__ __forceinline__ void dq_cta(const BwdMaps &tm, const BwdParams &p, co
             // from the swizzled shared tile (16-byte chunk c of row r sits at c ^ (r & 7))
             // into TMEM columns as packed bf16 pairs
             ok = wait_abort_warp(bar_qd, 0, p.err, kSiteBwQD, abort_flag);
-            if (ok) {
-                const uint8_t *tile = smem + C::kFixedOff + h * C::kTileBytes;
-#pragma unroll
-                for (int cb = 0; cb < D / 64; ++cb) {
-                    const uint8_t *row = tile + cb * (BT * 128) + r * 128;
-                    uint32_t wv[32];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(row + ((c ^ (r & 7)) << 4));
-                        wv[4 * c] = v.x;
-                        wv[4 * c + 1] = v.y;
-                        wv[4 * c + 2] = v.z;
-                        wv[4 * c + 3] = v.w;
-                    }
-                    tmem_st32(tmem + lane_off + (h ? kColDO : kColQ) + cb * 32, wv);
-                }
-                tmem_wait_st();
-            }
+            if (ok)
+                tile_row_to_tmem<D>(smem + C::kFixedOff + h * C::kTileBytes, r, tmem + lane_off + (h ? kColDO : kColQ));
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_qtm);

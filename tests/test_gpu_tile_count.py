@@ -87,3 +87,12 @@ def test_counts_match_the_needed_tiles(B, H, N, d, causal, key_len):
     if key_len is None and not causal:
         T = -(-N // TILE)
         assert (c == T * T).all()
+
+
+def test_headline_shape_counts_2080():
+    """The causal B1 H32 N8192 d128 prefill: T = 64 tiles a side, T(T+1)/2 = 2080 tile
+    products per (b, h) instead of 4096."""
+    T = 8192 // TILE
+    assert _needed_tiles(8192, True, None) == T * (T + 1) // 2 == 2080
+    c = _run(1, 32, 8192, 128, True, seed=2)
+    assert (c == 2080).all(), c

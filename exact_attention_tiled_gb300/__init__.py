@@ -19,7 +19,7 @@ import os
 import threading
 
 __all__ = ["fa_forward", "fa_forward_host", "fa_forward_host_workspace_bytes", "fa_forward_fp8", "fa_backward", "fa_backward_workspace_bytes", "fa_decode", "fa_decode_paged", "fa_decode_plan", "fa_decode_workspace_bytes",
-           "fa_device_error", "fa_get_last_device_error", "FaError", "library", "library_path", "STATUS"]
+           "fa_device_error", "fa_get_last_device_error", "fa_shutdown", "FaError", "library", "library_path", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libfa.so")
@@ -95,6 +95,8 @@ def library():
         lib.fa_get_last_device_error.argtypes = []
         lib.fa_get_last_device_error.restype = _i
         lib.fa_version.restype = _i
+        lib.fa_shutdown.argtypes = []
+        lib.fa_shutdown.restype = _i
         lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
         lib.fa_selftest_wait_timeout.restype = _i
         _lib = lib
@@ -435,3 +437,11 @@ def fa_device_error(clear=True):
 def fa_get_last_device_error():
     """Status of the device error word, which is then reset; synchronises the device."""
     return int(library().fa_get_last_device_error())
+
+
+def fa_shutdown():
+    """Release the library's streams, events and per-device lookups (status code).
+
+    Call with no other library call running; the next call sets them up again.
+    """
+    return int(library().fa_shutdown())

@@ -198,7 +198,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 101; }
 
 const char *fa_status_string(fa_status s) {
     switch (s) {
@@ -586,13 +586,29 @@ struct HostStreams {
     std::mutex enqueue;
 };
 
+// fa_forward_host's streams and events, created on a device's first call and
+// kept until fa_shutdown
+std::mutex g_host_mu;
+HostStreams *g_host[kMaxDevices] = {};
+
+void destroy_host_streams(HostStreams *h) {
+    cudaStreamDestroy(h->up);
+    for (int i = 0; i < kHostSlots; ++i) {
+        cudaStreamDestroy(h->st[i]);
+        cudaEventDestroy(h->h2d[i]);
+        cudaEventDestroy(h->d2h[i]);
+    }
+    cudaEventDestroy(h->start);
+    delete h;
+}
+
 cudaError_t host_streams(HostStreams **out) {
-    static std::mutex mu;
-    static HostStreams *per_dev[64] = {};
+    auto &per_dev = g_host;
+    auto &mu = g_host_mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!per_dev[dev]) {
         HostStreams *h = new HostStreams;
@@ -704,3 +720,41 @@ fa_status fa_forward_host(const void *Qh, const void *Kh, const void *Vh, void *
 }
 
 }  // extern "C"
+
+extern "C" fa_status fa_shutdown(void) {
+    fa_status st = FA_OK;
+    {
+        std::lock_guard<std::mutex> lock(g_host_mu);
+        int cur = -1;
+        bool have_cur = false;
+        for (int dev = 0; dev < kMaxDevices; ++dev) {
+            HostStreams *h = g_host[dev];
+            if (!h) continue;
+            if (!have_cur) have_cur = cudaGetDevice(&cur) == cudaSuccess;
+            // the calls that used these streams are complete before they go away
+            if (cudaSetDevice(dev) != cudaSuccess) {
+                st = FA_ERR_CUDA;
+            } else {
+                cudaError_t e = cudaStreamSynchronize(h->up);
+                for (int i = 0; i < kHostSlots; ++i) {
+                    const cudaError_t ei = cudaStreamSynchronize(h->st[i]);
+                    if (e == cudaSuccess) e = ei;
+                }
+                if (e != cudaSuccess) st = FA_ERR_CUDA;
+                destroy_host_streams(h);
+            }
+            g_host[dev] = nullptr;
+        }
+        if (have_cur && cur >= 0) cudaSetDevice(cur);
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (int dev = 0; dev < kMaxDevices; ++dev) {
+            g_err_ptr[dev] = nullptr;
+            g_sm_count[dev] = 0;
+            g_decode_ctas[dev][0] = g_decode_ctas[dev][1] = 0;
+        }
+    }
+    fa::reset_noalloc_addresses();
+    return st;
+}

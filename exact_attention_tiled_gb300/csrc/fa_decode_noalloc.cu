@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "../../include/fa.h"
+#include "fa_internal.h"
 
 namespace {
 
@@ -43,6 +44,13 @@ fa_status scratch_address(void **out) {
 }
 
 }  // namespace
+
+namespace fa {
+void reset_noalloc_addresses() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < kMaxDevices; ++i) g_scratch_addr[i] = nullptr;
+}
+}  // namespace fa
 
 extern "C" FA_API fa_status fa_decode_noalloc(const void *q, const void *Kcache, const void *Vcache,
                                               const int32_t *seqlens, const int32_t *seqlens_host, void *O,

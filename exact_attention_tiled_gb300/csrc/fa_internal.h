@@ -55,6 +55,8 @@ struct PrefillParams {
 cudaError_t launch_prefill(const PrefillParams &p, int d, cudaStream_t stream);
 // SM count of the current device (looked up once per device).
 cudaError_t current_sm_count(int *out);
+// Forget the fa_decode_noalloc array's per-device addresses (fa_shutdown).
+void reset_noalloc_addresses();
 // E4M3 -> bf16 (exact) for n elements; n a multiple of 8, both pointers 16-byte aligned.
 cudaError_t launch_e4m3_to_bf16(const void *src, void *dst, long long n, cudaStream_t stream);
 

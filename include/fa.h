@@ -289,8 +289,8 @@ FA_API fa_status fa_decode_plan(int B, int H, int Lmax, int d, int num_splits,
  *     nothing; use fa_decode with your own workspace for it.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
- *     The address is kept for the life of the process: after a
- *     cudaDeviceReset() it is stale, as is the device error word's.
+ *     The address is kept until fa_shutdown(); after a cudaDeviceReset()
+ *     without fa_shutdown() first it is stale, as is the device error word's.
  *   - Every call on a device uses the same array.  Nothing in it needs to
  *     start at zero (each partial is written before it is read), but two
  *     calls that overlap on the GPU, e.g. on two streams, race on it: order
@@ -374,6 +374,21 @@ FA_API fa_status fa_get_last_device_error(void);
  * fa_device_error() returns FA_ERR_DEVICE_TIMEOUT with *site = 0x301.
  */
 FA_API fa_status fa_selftest_wait_timeout(unsigned limit_us, fa_stream_t stream);
+
+/*
+ * fa_shutdown -- release what the library keeps between calls.  (No
+ * counterpart on the pages: the resource lifetime of this boundary.)
+ * That is the streams and events fa_forward_host creates per device, and
+ * the per-device lookups every call shares: the device error word's and the
+ * fa_decode_noalloc array's addresses, the SM count and the decode CTAs per
+ * SM.  It first waits for the work queued on those streams.  Call it with no
+ * other library call running on any host thread; the next call sets
+ * everything up again.  Call it before cudaDeviceReset(), after which the
+ * cached addresses would be stale.  Returns FA_ERR_CUDA if a device could not
+ * be selected or synchronised (the remaining state is still released), else
+ * FA_OK; with nothing cached it touches no device.
+ */
+FA_API fa_status fa_shutdown(void);
 
 /* Library ABI version (major * 100 + minor). */
 FA_API int fa_version(void);

@@ -35,7 +35,7 @@ def test_header_declares_the_api():
     # and this library's additions
     assert {"fa_decode_plan", "fa_decode_workspace_bytes_for_lengths", "fa_device_error", "fa_version",
             "fa_decode_paged", "fa_backward", "fa_forward_fp8", "fa_forward_host",
-            "fa_decode_noalloc"} <= set(names)
+            "fa_decode_noalloc", "fa_shutdown"} <= set(names)
 
 
 def test_boundary_signatures(lib):
@@ -58,6 +58,14 @@ def test_boundary_signatures(lib):
     import torch
     if not torch.cuda.is_available():
         assert g() == 3
+
+
+def test_shutdown_with_nothing_cached_touches_no_device(lib):
+    """fa_shutdown before any call that caches state: FA_OK, even without a GPU, and twice."""
+    lib.fa_shutdown.argtypes = []
+    lib.fa_shutdown.restype = ctypes.c_int
+    assert lib.fa_shutdown() == 0
+    assert lib.fa_shutdown() == 0
 
 
 def test_library_exports_every_declared_symbol(lib):

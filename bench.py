@@ -737,9 +737,11 @@ def main():
         torch.distributed.init_process_group("nccl")
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
-        v, threads, desc = oracle_sample(args.cpu_seconds)
-        res["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                               "sample": desc, **oracle_extras(threads)}
+        # the oracle baseline on the host cores belongs to the single-GPU line only
+        if world == 1:
+            v, threads, desc = oracle_sample(args.cpu_seconds)
+            res["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                   "sample": desc, **oracle_extras(threads)}
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch

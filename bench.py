@@ -418,6 +418,19 @@ def run_ours(args, rank, world, local_rank):
         others[name] = {"ms": round(ms, 4), "flops": fl, "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
                         "frac_of_bf16_peak": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                         "kernels": "bwd_pre + bwd_main (dK/dV and dQ CTAs in one grid; S and dP recomputed in both)"}
+        if d_ == 64:
+            # fa_backward_atomic_dq: dQ accumulated by the dK/dV CTAs with TMA reductions
+            # (d = 64 only); not bitwise reproducible in dQ
+            wsa = torch.empty(fa.library().fa_backward_atomic_dq_workspace_bytes(B_, H_, N_, d_), device=dev,
+                              dtype=torch.uint8)
+            ms = timed(lambda: fa.fa_backward(Qb, Kb, Vb, Ob, dOb, Lb, causal=causal_, dQ=dQb, dK=dKb, dV=dVb,
+                                              workspace=wsa, atomic_dq=True))
+            others[name + "_atomic_dq"] = {
+                "ms": round(ms, 4), "flops": fl, "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+                "frac_of_bf16_peak": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                "kernels": "memset + bwd_pre + bwd_main (dK/dV CTAs also form dQ partials, added into an fp32 "
+                           "copy by TMA reductions) + dq_finalize"}
+            del wsa
         del Qb, Kb, Vb, dOb, Ob, Lb, dQb, dKb, dVb
     st, site = fa.fa_device_error(clear=True)
     if st != 0:

@@ -71,6 +71,10 @@ def library():
         lib.fa_backward.restype = _i
         lib.fa_backward_workspace_bytes.argtypes = [_i, _i, _i, _i]
         lib.fa_backward_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_backward_atomic_dq.argtypes = lib.fa_backward.argtypes
+        lib.fa_backward_atomic_dq.restype = _i
+        lib.fa_backward_atomic_dq_workspace_bytes.argtypes = [_i, _i, _i, _i]
+        lib.fa_backward_atomic_dq_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_forward_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _vp,
                                         ctypes.c_size_t, _vp]
         lib.fa_forward_fp8.restype = _i
@@ -288,11 +292,13 @@ def fa_backward_workspace_bytes(B, H, N, d):
 
 
 def fa_backward(Q, K, V, O, dO, L, causal=False, scale=None, key_len=None, dQ=None, dK=None, dV=None,
-                workspace=None, stream=None):
+                workspace=None, stream=None, atomic_dq=False):
     """Gradients (dQ, dK, dV) of exact attention; all bf16 [B, H, N, d] on the GPU.
 
     O and L are the outputs of fa_forward for the same Q, K, V, causal, scale
-    and key_len; dO is the upstream gradient of O.
+    and key_len; dO is the upstream gradient of O.  atomic_dq=True (d = 64)
+    calls fa_backward_atomic_dq: dQ accumulated by fp32 atomics, less work,
+    dQ not bitwise reproducible.
     """
     torch = _torch()
     for n, t in (("Q", Q), ("K", K), ("V", V), ("O", O), ("dO", dO)):
@@ -312,15 +318,16 @@ def fa_backward(Q, K, V, O, dO, L, causal=False, scale=None, key_len=None, dQ=No
     dV = torch.empty_like(Q) if dV is None else dV
     for n, t in (("dQ", dQ), ("dK", dK), ("dV", dV)):
         _check_bf16(n, t, 4)
-    need = library().fa_backward_workspace_bytes(B, H, N, d)
+    lib = library()
+    need = (lib.fa_backward_atomic_dq_workspace_bytes if atomic_dq else lib.fa_backward_workspace_bytes)(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), device=Q.device, dtype=torch.uint8)
-    st = library().fa_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK),
-                               _ptr(dV), B, H, N, d, int(bool(causal)),
-                               float(scale) if scale is not None else 0.0, _ptr(key_len), _ptr(workspace),
-                               workspace.numel(), _stream_handle(stream))
+    fn, name = (lib.fa_backward_atomic_dq, "fa_backward_atomic_dq") if atomic_dq else (lib.fa_backward, "fa_backward")
+    st = fn(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(dQ), _ptr(dK), _ptr(dV), B, H, N, d,
+            int(bool(causal)), float(scale) if scale is not None else 0.0, _ptr(key_len), _ptr(workspace),
+            workspace.numel(), _stream_handle(stream))
     if st != 0:
-        raise FaError(st, "fa_backward")
+        raise FaError(st, name)
     return dQ, dK, dV
 
 

@@ -420,14 +420,27 @@ size_t fa_backward_workspace_bytes(int B, int H, int N, int d) {
     return align256(static_cast<size_t>(B) * H * N * sizeof(float));
 }
 
-fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O, const void *dO,
-                      const float *L, void *dQ, void *dK, void *dV, int B, int H, int N, int d, int causal,
-                      float scale, const int32_t *key_len, void *workspace, size_t workspace_bytes,
-                      fa_stream_t stream) {
+size_t fa_backward_atomic_dq_workspace_bytes(int B, int H, int N, int d) {
+    const size_t dbytes = fa_backward_workspace_bytes(B, H, N, d);
+    if (d != 64 || dbytes == 0) return 0;
+    return dbytes + align256(static_cast<size_t>(B) * H * N * d * sizeof(float));
+}
+
+}  // extern "C"
+
+namespace {
+
+// fa_backward and fa_backward_atomic_dq: the same validation and parameters; the
+// second also hands the dK/dV CTAs an fp32 dQ accumulator after D in the workspace.
+fa_status backward_impl(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *L,
+                        void *dQ, void *dK, void *dV, int B, int H, int N, int d, int causal, float scale,
+                        const int32_t *key_len, void *workspace, size_t workspace_bytes, fa_stream_t stream,
+                        bool atomic_dq) {
     if (!Q || !K || !V || !O || !dO || !L || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (atomic_dq && d != 64) return FA_ERR_UNSUPPORTED;
     if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(dO, 16) ||
         !aligned(dQ, 16) || !aligned(dK, 16) || !aligned(dV, 16) || !aligned(L, 4) ||
         (key_len && !aligned(key_len, 4)))
@@ -435,7 +448,8 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
     if (static_cast<long long>(B) * H * N > (1ll << 40)) return FA_ERR_UNSUPPORTED;
     if (!(std::isfinite(scale))) return FA_ERR_INVALID_ARG;
     if (scale <= 0.f) scale = 1.0f / std::sqrt(static_cast<float>(d));
-    const size_t need = fa_backward_workspace_bytes(B, H, N, d);
+    const size_t need =
+        atomic_dq ? fa_backward_atomic_dq_workspace_bytes(B, H, N, d) : fa_backward_workspace_bytes(B, H, N, d);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return FA_ERR_WORKSPACE;
 
     unsigned *err = nullptr;
@@ -462,8 +476,30 @@ fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = err;
+    if (atomic_dq)
+        p.dq_accum = reinterpret_cast<float *>(static_cast<char *>(workspace) + fa_backward_workspace_bytes(B, H, N, d));
     if (launch_backward(p, d, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
     return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_backward(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                      const float *L, void *dQ, void *dK, void *dV, int B, int H, int N, int d, int causal,
+                      float scale, const int32_t *key_len, void *workspace, size_t workspace_bytes,
+                      fa_stream_t stream) {
+    return backward_impl(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, d, causal, scale, key_len, workspace,
+                         workspace_bytes, stream, false);
+}
+
+fa_status fa_backward_atomic_dq(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                                const float *L, void *dQ, void *dK, void *dV, int B, int H, int N, int d,
+                                int causal, float scale, const int32_t *key_len, void *workspace,
+                                size_t workspace_bytes, fa_stream_t stream) {
+    return backward_impl(Q, K, V, O, dO, L, dQ, dK, dV, B, H, N, d, causal, scale, key_len, workspace,
+                         workspace_bytes, stream, true);
 }
 
 }  // extern "C"

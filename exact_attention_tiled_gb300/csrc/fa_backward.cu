@@ -31,9 +31,15 @@
 //     warpgroups, and dQ += dS K_j in TMEM.  Computing dQ in its own pass
 //     (recomputing S and dP) keeps every gradient element written by exactly
 //     one CTA: no atomics, and the result does not depend on scheduling.
+// The dQ-accumulating variant (fa_backward_atomic_dq, d = 64) runs dK/dV
+// CTAs only: each also forms dQ_i += dS_i K_j for every query tile it meets
+// (dS^T copied to shared memory as the A operand) and adds it into an fp32
+// dQ through TMA reductions; a last kernel scales and rounds it.  Less work,
+// but the order of the fp32 additions depends on scheduling.
 // Warp roles in both kinds of CTA (640 threads): warp 0 lane 0 issues the
 // TMA copies, warp 1 is the MMA warp (converged, one elected lane issues),
-// warps 4-19 are four compute warpgroups, one thread per TMEM lane (tile row).
+// warps 4-19 are four compute warpgroups, one thread per TMEM lane (tile row);
+// in the dQ variant warp 2 lane 0 issues the reductions.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -53,16 +59,17 @@ constexpr int BT = 128;              // rows of a query or key tile (MMA M and N
 // columns in the dQ kernel); warpgroups 2 hf and 2 hf + 1 serve half-step hf
 constexpr int kComputeGroups = 4;
 constexpr int kBwdThreads = 128 * (1 + kComputeGroups);
-constexpr int kProd = 0, kMma = 1, kFirstCompute = 4;
+constexpr int kProd = 0, kMma = 1, kDqWarp = 2, kFirstCompute = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum {
     kSiteBwKV = 0x401, kSiteBwQD = 0x402, kSiteBwS = 0x403, kSiteBwP = 0x404, kSiteBwDone = 0x405,
-    kSiteBwEmpty = 0x406, kSiteBwDrain = 0x407
+    kSiteBwEmpty = 0x406, kSiteBwDrain = 0x407, kSiteBwDqFree = 0x408, kSiteBwDqd = 0x409, kSiteBwStage = 0x40a
 };
 
 struct BwdMaps {
     CUtensorMap q, k, v, dO, dq, dk, dv;
+    CUtensorMap dqa;   // fp32 dQ accumulator (the dQ-accumulating variant only)
 };
 
 // Row r, 16-byte chunk kc (8 bf16 columns) of a 128-row tile in the 128-byte
@@ -133,11 +140,24 @@ struct BwdCfg {
     static constexpr int kStageOff = 2 * kTileBytes;
     static constexpr int kVecOff = kStageOff + kStages * 2 * kTileBytes;
     static constexpr int kBarOff = kVecOff + kStages * 2 * BT * 4;
-    static constexpr int kNumBars = 16;
+    static constexpr int kNumBars = 20;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     // at least 120 KB, so one CTA per SM: each allocates all 512 TMEM columns
     static constexpr int kSmemUsed = kMiscOff + 16 + 1024;
     static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
+};
+
+// The dQ-accumulating variant of the dK/dV CTA (d = 64) adds two shared buffers of
+// dS^T for a query tile (128 keys x 128 queries bf16, as the A operand of dQ = dS K:
+// queries contiguous, two 64-query column blocks of 128 x 128 bytes), after the
+// CTA's other shared state.
+template <int D>
+struct AtomicDqShape {
+    using C = BwdCfg<D, 3>;
+    static constexpr int kDsBytes = BT * BT * 2;
+    static constexpr int kDsOff = (C::kMiscOff + 16 + 1023) / 1024 * 1024;
+    static constexpr int kSmemBytes = kDsOff + 2 * kDsBytes + 1024;
+    static_assert(D != 64 || kSmemBytes <= 227 * 1024, "shared memory per CTA");   // used at d = 64 only
 };
 
 // Both main kernels run a step (one 128-row tile of the streamed operand) as two
@@ -185,9 +205,12 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *O, co
 // dK, dV of key tile jt of (batch, head) bh: one CTA (key tile 0 is the
 // heaviest under causal masking: key tile j meets the query tiles i >= j).
 // ---------------------------------------------------------------------------
-template <int D>
+// kAtomicDQ (d = 64 only): the CTA also forms dQ_i += dS_i K_j for every query tile
+// it meets and adds it into p.dq_accum with fp32 vector atomics, so no dQ CTAs run.
+template <int D, bool kAtomicDQ = false>
 __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, const int bh, const int jt) {
     using C = BwdCfg<D, HalfStepShape<D>::kStages>;
+    static_assert(!kAtomicDQ || D == 64, "the dQ accumulator fits in TMEM at d = 64 only");
     // At d = 64 this kernel keeps two half-step buffers and copies K_j and V_j into
     // TMEM (packed bf16 rows, one key per lane), so S^T = K Q_h^T and dP^T = V dO_h^T
     // are TS products that read only Q_h and dO_h from shared memory (measured: d = 64
@@ -198,6 +221,9 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
     constexpr uint32_t kColGrad = 128u * NB;
     constexpr uint32_t kColK = kColGrad + 2 * D, kColV = kColK + D / 2;
     static_assert(!kKvTmem || kColV + D / 2 <= 512, "TMEM columns");
+    // dQ partial of the current query tile (queries on the lanes), after K_j and V_j
+    constexpr uint32_t kColDq = kColV + D / 2;
+    static_assert(!kAtomicDQ || kColDq + D <= 512, "TMEM columns");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -219,7 +245,17 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
     auto bar_ps = [&](int bf) { return bars + 8u * (1 + 2 * C::kStages + NB + bf); };
     const uint32_t bar_done = bars + 8u * (1 + 2 * C::kStages + 2 * NB);
     const uint32_t bar_ktm = bar_done + 8u;   // K_j, V_j are in TMEM
-    static_assert(1 + 2 * C::kStages + 2 * NB + 2 <= C::kNumBars, "barrier slots");
+    // dQ variant: bar_dqd(b) -- the dQ products of a query tile n with n % 2 == b are
+    // complete; bar_dq_free -- every compute warp has read the previous tile's dQ out
+    // of TMEM; bar_stage_full -- every compute warp has staged the tile's dQ (fp32)
+    // in the tile's dS buffer; bar_stage_free(b) -- the reduction of the staged dQ
+    // of the last tile that used buffer b has read it
+    auto bar_dqd = [&](int b) { return bar_ktm + 8u * (1 + b); };
+    const uint32_t bar_dq_free = bar_ktm + 24u;
+    const uint32_t bar_stage_full = bar_ktm + 32u;
+    auto bar_stage_free = [&](int b) { return bar_ktm + 8u * (5 + b); };
+    static_assert(1 + 2 * C::kStages + 2 * NB + 2 + (kAtomicDQ ? 6 : 0) <= C::kNumBars, "barrier slots");
+    auto ds_buf = [&](int b) { return sbase + AtomicDqShape<D>::kDsOff + b * AtomicDqShape<D>::kDsBytes; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
 
@@ -246,6 +282,14 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
         }
         mbar_init(bar_done, 1);
         mbar_init(bar_ktm, 8);
+        if (kAtomicDQ) {
+            mbar_init(bar_dqd(0), 1);
+            mbar_init(bar_dqd(1), 1);
+            mbar_init(bar_dq_free, 16);
+            mbar_init(bar_stage_full, 16);
+            mbar_init(bar_stage_free(0), 1);
+            mbar_init(bar_stage_free(1), 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -392,11 +436,52 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
                 issue_grad(u);
                 if (u & 1) mma_commit_warp(bar_empty((u >> 1) % C::kStages));   // Q_i, dO_i read
                 if (u + NB < nhalf) ok = issue_sdp(u + NB);
+                if constexpr (kAtomicDQ) {
+                    if ((u & 1) && ok) {
+                        // dQ_i (queries on the lanes) = dS_i K_j: A = dS^T of both halves from
+                        // shared memory (published by the two ps barriers), MN-major; B = K_j,
+                        // d contiguous.  The TMEM accumulator is free once every compute warp
+                        // has read the previous tile's.
+                        const int n = u >> 1;
+                        if (n > 0) ok = wait_abort_warp(bar_dq_free, (n - 1) & 1, p.err, kSiteBwDqFree, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        constexpr uint32_t idesc_dq = idesc_bf16_f32(BT, D, 1, 1);
+                        const uint64_t ad = sdesc_sw128(ds_buf(n & 1), BT * 128, 1024);
+                        const uint64_t bd = sdesc_sw128(k_smem, BT * 128, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < BT / 16; ++kk) {
+                            const uint32_t off = (kk * 2048) >> 4;   // 16 key rows
+                            mma_ss_warp(tmem + kColDq, ad + off, bd + off, idesc_dq, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit_warp(bar_dqd(n & 1));
+                    }
+                }
             }
             // every MMA has completed before the gradients are read and TMEM is freed
             mma_commit_warp(bar_done);
             mbar_wait(bar_done, 0, p.err, kSiteBwDone);
             __syncwarp();
+        }
+    } else if (kAtomicDQ && warp == kDqWarp) {
+        // ================================================= dQ reduction warp (dQ variant)
+        // Once every compute warp has staged query tile m's dQ partial, add it into the
+        // fp32 accumulator (rows past N are skipped by the tensor map) and release the
+        // buffer as soon as the reduction has read it.
+        if (lane == 0 && nsteps > 0) {
+            prefetch_tmap(&tm.dqa);
+            for (int m = 0; m < nsteps; ++m) {
+                if (!wait_abort(bar_stage_full, m & 1, p.err, kSiteBwStage, abort_flag)) break;
+                const uint32_t stg = ds_buf(m & 1);
+#pragma unroll
+                for (int cb = 0; cb < D / 32; ++cb)
+                    tma_reduce_add_3d(&tm.dqa, stg + cb * (BT * 128), cb * 32, (i_lo + m) * BT, bh);
+                bulk_commit_group();
+                bulk_wait_group_read0();
+                mbar_arrive(bar_stage_free(m & 1));
+            }
+            // every addition has reached global memory before the CTA exits
+            bulk_wait_group0();
         }
     } else if (warp >= kFirstCompute) {
         // ================================================= compute warpgroups
@@ -423,6 +508,30 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_ktm);
         }
+        // dQ variant: this thread's 16 columns (16 h ..) of query tile m's dQ partial, on
+        // its lane (query row r of the tile), staged as fp32 in the tile's dS buffer (the
+        // dQ products are done with it) in the 128-byte swizzled layout of the
+        // accumulator's tensor map; warp kDqWarp adds the staged tile into p.dq_accum
+        auto dq_readout = [&](int m) -> bool {
+            if (!wait_abort_warp(bar_dqd(m & 1), (m >> 1) & 1, p.err, kSiteBwDqd, abort_flag)) return false;
+            tc_fence_after();
+            __syncwarp();
+            uint32_t a[16];
+            tmem_ld16(tmem + lane_off + kColDq + 16 * h, a);
+            tmem_wait_ld();
+            reg_fence(a);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_dq_free);
+            const uint32_t stg = ds_buf(m & 1) + (h >> 1) * (BT * 128);   // 32 fp32 columns per block
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                st_shared_v4(swz_chunk(stg, r, 4 * (h & 1) + v), a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_stage_full);
+            return true;
+        };
         for (int n = 0; n < nsteps && ok; ++n) {
             const int s = n % C::kStages;
             const int q0 = (i_lo + n) * BT;
@@ -489,10 +598,35 @@ __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, 
             half(h, 1, sb, db, pp, dp);
             tmem_st16(tmem + lane_off + col, pp);
             tmem_st16(tmem + lane_off + col + 64, dp);
+            if constexpr (kAtomicDQ) {
+                // dS^T row r, query columns 32 h .. 32 h + 31, into this tile's shared dS
+                // buffer, for the dQ products (the ps arrive below publishes it to them);
+                // the buffer last held tile n - 2's staged dQ, whose reduction must have read it
+                if (n >= 2 && !wait_abort_warp(bar_stage_free(n & 1), ((n - 2) >> 1) & 1, p.err, kSiteBwStage,
+                                               abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dsb = ds_buf(n & 1) + (h >> 1) * (BT * 128);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    st_shared_v4(swz_chunk(dsb, r, 4 * (h & 1) + c), dp[4 * c], dp[4 * c + 1], dp[4 * c + 2],
+                                 dp[4 * c + 3]);
+                fence_proxy_async_shared();
+            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_ps(u % NB));
+            if constexpr (kAtomicDQ) {
+                if (n > 0 && !dq_readout(n - 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+        }
+        if constexpr (kAtomicDQ) {
+            if (ok && nsteps > 0) ok = dq_readout(nsteps - 1);
         }
         // ---- epilogue: dV and dK (x scale) to bf16; keys with no step get zeros
         if (ok && nsteps > 0) {
@@ -835,20 +969,40 @@ __device__ __forceinline__ void dq_cta(const BwdMaps &tm, const BwdParams &p, co
 // dK/dV CTAs, the others dQ CTAs.  The two halves are independent (both need
 // only D), so dQ CTAs fill the SMs that the dK/dV half leaves idle in its last
 // wave instead of waiting for a second launch.
-template <int D>
+template <int D, bool kAtomicDQ = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
     const int T = (p.N + BT - 1) / BT;
     const int y = static_cast<int>(blockIdx.y);
-    if (y < T)
-        dkdv_cta<D>(tm, p, static_cast<int>(blockIdx.x), y);
-    else
-        dq_cta<D>(tm, p, static_cast<int>(blockIdx.x), y - T);
+    if constexpr (kAtomicDQ) {
+        dkdv_cta<D, true>(tm, p, static_cast<int>(blockIdx.x), y);
+    } else {
+        if (y < T)
+            dkdv_cta<D>(tm, p, static_cast<int>(blockIdx.x), y);
+        else
+            dq_cta<D>(tm, p, static_cast<int>(blockIdx.x), y - T);
+    }
+}
+
+// dQ = bf16(scale * dQ accumulated in fp32), 8 elements per thread
+__global__ void __launch_bounds__(256) dq_finalize_kernel(const float4 *acc, uint4 *dq, float scale, long long n8) {
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    dq[i] = make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
+                       pack_bf16(b.x * scale, b.y * scale), pack_bf16(b.z * scale, b.w * scale));
 }
 
 template <int D>
 cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     const long long rows = static_cast<long long>(p.B) * p.H * p.N;
+    constexpr bool kCanAtomic = D == 64;
+    const bool atomic_dq = p.dq_accum != nullptr;
+    if (atomic_dq && !kCanAtomic) return cudaErrorInvalidValue;
+    if (atomic_dq) {
+        const cudaError_t e = cudaMemsetAsync(p.dq_accum, 0, static_cast<size_t>(rows) * D * sizeof(float), stream);
+        if (e != cudaSuccess) return e;
+    }
     {
         constexpr int LPR = D / 8;
         const long long threads = rows * LPR;
@@ -867,15 +1021,23 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
         !make_map(&tm.dq, p.dQ, BH, p.N, D) || !make_map(&tm.dk, p.dK, BH, p.N, D) ||
         !make_map(&tm.dv, p.dV, BH, p.N, D))
         return cudaErrorInvalidValue;
-    const int smem = BwdCfg<D, HalfStepShape<D>::kStages>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (atomic_dq && !make_map_f32(&tm.dqa, p.dq_accum, BH, p.N, D)) return cudaErrorInvalidValue;
+    int smem = BwdCfg<D, HalfStepShape<D>::kStages>::kSmemBytes;
+    const void *kern = reinterpret_cast<const void *>(bwd_main_kernel<D>);
+    if constexpr (kCanAtomic) {
+        if (atomic_dq) {
+            smem = AtomicDqShape<D>::kSmemBytes;
+            kern = reinterpret_cast<const void *>(bwd_main_kernel<D, true>);
+        }
+    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int T = (p.N + BT - 1) / BT;
     if (2ll * T > 65535) return cudaErrorInvalidValue;
     // launched as a programmatic dependent of bwd_pre_kernel: its CTAs set up
     // (barriers, TMEM, the first K/V or Q/dO loads) while D is still being written
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(BH), static_cast<unsigned>(2 * T), 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(BH), static_cast<unsigned>(atomic_dq ? T : 2 * T), 1);
     cfg.blockDim = dim3(kBwdThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
@@ -884,6 +1046,18 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if constexpr (kCanAtomic) {
+        if (atomic_dq) {
+            e = cudaLaunchKernelEx(&cfg, bwd_main_kernel<D, true>, tm, p);
+            if (e != cudaSuccess) return e;
+            const long long n8 = rows * D / 8;
+            const long long blocks = (n8 + 255) / 256;
+            if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+            dq_finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+                reinterpret_cast<const float4 *>(p.dq_accum), static_cast<uint4 *>(p.dQ), p.scale, n8);
+            return cudaGetLastError();
+        }
+    }
     return cudaLaunchKernelEx(&cfg, bwd_main_kernel<D>, tm, p);
 }
 

@@ -72,6 +72,7 @@ struct BwdParams {
     float scale;                      // score multiplier
     float scale_log2;                 // scale * log2(e)
     unsigned *err;
+    float *dq_accum;                  // nullptr, or fp32 [B, H, N, d]: dQ accumulated by the dK/dV CTAs
 };
 
 cudaError_t launch_backward(const BwdParams &p, int d, cudaStream_t stream);

@@ -143,6 +143,13 @@ __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int
                  "r"(src), "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
 }
+// Element-wise fp32 addition of a shared-memory tile into global memory through
+// a tensor map (the additions happen in L2; rows outside the tensor are skipped).
+__device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(tmap), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // The shared-memory sources of this thread's committed bulk stores have been read.
 __device__ __forceinline__ void bulk_wait_group_read0() {

@@ -43,6 +43,22 @@ inline bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view [B*H][N][d] of an fp32 tensor; box = 32 columns (one 128-byte row) x
+// 128 rows x 1, 128-byte swizzle: the backward's dQ accumulator, which tiles of
+// dQ partials are added into by TMA reductions.
+inline bool make_map_f32(CUtensorMap *m, const void *base, int BH, int N, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || d % 32 != 0) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
+    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D view [B*H][N][d] of a one-byte (E4M3) tensor; box = 128 columns (one
 // 128-byte row) x 128 rows x 1, 128-byte swizzle.  d must be a multiple of 128.
 inline bool make_map_u8(CUtensorMap *m, const void *base, int BH, int N, int d) {

@@ -211,6 +211,34 @@ FA_API fa_status fa_backward(const void *Q, const void *K, const void *V, const 
 FA_API size_t fa_backward_workspace_bytes(int B, int H, int N, int d);
 
 /*
+ * fa_backward_atomic_dq -- fa_backward with dQ accumulated across key tiles by
+ * fp32 atomic additions.  (The pages compute dQ_i = scale sum_j dS_ij K_j by
+ * blocks, "Blocked gradient computation"; this entry point is a different order
+ * of that sum, not a different result.)
+ *
+ * The thread block of key tile j, which already holds K_j and forms dS for
+ * every query tile it meets, also forms dQ_i += dS_i K_j in TMEM and adds it
+ * into an fp32 copy of dQ in the workspace; a last kernel scales it and
+ * rounds it to bf16.  No second pass recomputes S, dP and dS per query tile,
+ * so it does less work than fa_backward; but the order of the fp32 additions
+ * into dQ depends on scheduling, so dQ may differ from run to run in its last
+ * bits (dK and dV do not: they are produced as in fa_backward).
+ *
+ * Arguments as fa_backward, except: d must be 64 (FA_ERR_UNSUPPORTED
+ * otherwise: at d = 128 the dQ accumulator does not fit beside dK and dV in
+ * tensor memory), and the workspace holds at least
+ * fa_backward_atomic_dq_workspace_bytes() bytes (D, then the fp32 dQ).
+ */
+FA_API fa_status fa_backward_atomic_dq(const void *Q, const void *K, const void *V, const void *O,
+                                       const void *dO, const float *L, void *dQ, void *dK, void *dV,
+                                       int B, int H, int N, int d, int causal, float scale,
+                                       const int32_t *key_len, void *workspace, size_t workspace_bytes,
+                                       fa_stream_t stream);
+
+/* Workspace bytes fa_backward_atomic_dq needs (0 for arguments it would reject). */
+FA_API size_t fa_backward_atomic_dq_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * fa_decode -- split-KV single-query attention (Flash-Decoding).
  *
  *   q             bf16 [B, H, d]: one query per (b, h).

@@ -35,7 +35,7 @@ def test_header_declares_the_api():
     # and this library's additions
     assert {"fa_decode_plan", "fa_decode_workspace_bytes_for_lengths", "fa_device_error", "fa_version",
             "fa_decode_paged", "fa_backward", "fa_forward_fp8", "fa_forward_host",
-            "fa_decode_noalloc", "fa_shutdown"} <= set(names)
+            "fa_decode_noalloc", "fa_shutdown", "fa_backward_atomic_dq"} <= set(names)
 
 
 def test_boundary_signatures(lib):
@@ -283,6 +283,32 @@ def test_backward_rejects_bad_arguments_before_cuda(lib):
     assert _bwd(lib, wsb=16) == 4
     assert lib.fa_backward_workspace_bytes(2, 3, 1000, 128) == (2 * 3 * 1000 * 4 + 255) // 256 * 256
     assert lib.fa_backward_workspace_bytes(2, 3, 1000, 96) == 0
+
+
+def test_backward_atomic_dq_rejects_bad_arguments_before_cuda(lib):
+    f = lib.fa_backward_atomic_dq
+    f.restype = ctypes.c_int
+    wsb = lib.fa_backward_atomic_dq_workspace_bytes
+    wsb.argtypes = [ctypes.c_int] * 4
+    wsb.restype = ctypes.c_size_t
+
+    def call(**kw):
+        a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, dO=FAKE, L=FAKE, dQ=FAKE, dK=FAKE, dV=FAKE, B=1, H=2, N=256,
+                 d=64, causal=0, scale=0.0, kl=None, ws=FAKE, wsb=1 << 20)
+        a.update(kw)
+        return f(a["Q"], a["K"], a["V"], a["O"], a["dO"], a["L"], a["dQ"], a["dK"], a["dV"], a["B"], a["H"],
+                 a["N"], a["d"], a["causal"], ctypes.c_float(a["scale"]), a["kl"], a["ws"], a["wsb"], None)
+
+    assert call(dQ=None) == 1
+    assert call(causal=2) == 1
+    assert call(d=128) == 2      # the dQ accumulator fits in TMEM at d = 64 only
+    assert call(d=32) == 2
+    # D, then the fp32 dQ accumulator: the plain backward's workspace is too small
+    need = wsb(1, 2, 256, 64)
+    assert need == lib.fa_backward_workspace_bytes(1, 2, 256, 64) + 1 * 2 * 256 * 64 * 4
+    assert call(wsb=lib.fa_backward_workspace_bytes(1, 2, 256, 64)) == 4
+    assert call(wsb=need - 1) == 4
+    assert wsb(1, 2, 256, 128) == 0 and wsb(0, 2, 256, 64) == 0
 
 
 def test_forward_fp8_rejects_bad_arguments_before_cuda(lib):

@@ -206,7 +206,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *O, co
 // heaviest under causal masking: key tile j meets the query tiles i >= j).
 // ---------------------------------------------------------------------------
 // kAtomicDQ (d = 64 only): the CTA also forms dQ_i += dS_i K_j for every query tile
-// it meets and adds it into p.dq_accum with fp32 vector atomics, so no dQ CTAs run.
+// it meets and adds it into the fp32 accumulator p.dq_accum with TMA reductions
+// (through tm.dqa), so no dQ CTAs run.
 template <int D, bool kAtomicDQ = false>
 __device__ __forceinline__ void dkdv_cta(const BwdMaps &tm, const BwdParams &p, const int bh, const int jt) {
     using C = BwdCfg<D, HalfStepShape<D>::kStages>;

@@ -73,6 +73,14 @@ def test_atomic_dq_key_padding_and_empty_rows():
     assert np.all(got["dQ"][2] == 0)
 
 
+@pytest.mark.parametrize("N,key_len", [(300, [300, 129, 1]), (640, [500, 128, 640])])
+def test_atomic_dq_causal_with_key_padding(N, key_len):
+    Q, K, V, dO = _inputs(3, 2, N, 64, seed=1450 + N)
+    got = _both(Q, K, V, dO, True, key_len)
+    ref = oracle.sdpa_backward(Q, K, V, dO, causal=True, key_len=key_len, magnitudes=True)
+    _check(f"atomic dQ causal keypad N{N}", got, ref)
+
+
 def test_atomic_dq_batched_sampled_heads():
     """B8 H16 N2048 d64 (x0.5), the batched prefill shape; oracle on sampled heads."""
     B, H, N, d = 8, 16, 2048, 64

@@ -690,15 +690,17 @@ def run_profile_case(args):
         w3 = workloads.WORKLOADS["prefill_b8h16_n2048_d64"]
         Q, K, V = workloads.prefill_inputs(w3.B, w3.H, w3.N, w3.d, w3.seed, w3.amp, device=dev)
         run = lambda: fa.fa_forward(Q, K, V, causal=False)
-    elif args.profile == "backward":
-        # the batched d64 shape (B8 H16 N2048): ~0.3 GB on the device
+    elif args.profile in ("backward", "backward_atomic"):
+        # the batched d64 shape (B8 H16 N2048): ~0.3 GB on the device (plus the fp32 dQ
+        # of the dQ-accumulating variant)
         w3 = workloads.WORKLOADS["prefill_b8h16_n2048_d64"]
         Q, K, V = workloads.prefill_inputs(w3.B, w3.H, w3.N, w3.d, w3.seed, w3.amp, device=dev)
         gb = torch.Generator(device=dev)
         gb.manual_seed(w3.seed + 1000)
         dO = torch.randn(Q.shape, generator=gb, device=dev, dtype=torch.float32).to(torch.bfloat16)
         O, L = fa.fa_forward(Q, K, V)
-        run = lambda: fa.fa_backward(Q, K, V, O, dO, L)
+        atomic = args.profile == "backward_atomic"
+        run = lambda: fa.fa_backward(Q, K, V, O, dO, L, atomic_dq=atomic)
     else:
         wd = workloads.WORKLOADS[DECODE]
         q, Kc, Vc = workloads.decode_inputs(wd.B, wd.H, wd.N, wd.d, wd.seed, device=dev)
@@ -722,7 +724,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["prefill", "prefill64", "prefill_fp8", "decode", "backward"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "prefill64", "prefill_fp8", "decode", "backward", "backward_atomic"],
+                    default=None,
                     help="only launch one kernel warmup+steps times (for ncu captures)")
     ap.add_argument("--record-traffic", nargs=3, metavar=("REPORT", "KERNEL", "NOTE"), default=None,
                     help="write DRAM bytes per launch of KERNEL from an ncu report to profiles/")

@@ -973,15 +973,25 @@ __device__ __forceinline__ void dq_cta(const BwdMaps &tm, const BwdParams &p, co
 template <int D, bool kAtomicDQ = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
-    const int T = (p.N + BT - 1) / BT;
-    const int y = static_cast<int>(blockIdx.y);
     if constexpr (kAtomicDQ) {
-        dkdv_cta<D, true>(tm, p, static_cast<int>(blockIdx.x), y);
+        // grid (B*H, T): every unit's key tile y, units innermost
+        dkdv_cta<D, true>(tm, p, static_cast<int>(blockIdx.x), static_cast<int>(blockIdx.y));
     } else {
+        const int T = (p.N + BT - 1) / BT;
+        // CTA order: (b, h) units in groups of p.head_group; inside a group the CTA
+        // kinds and tiles run in order, heaviest first, with the group's units innermost.
+        // With small groups the CTAs running at once touch few units' Q, K, V and dO,
+        // which then stay in L2.
+        const unsigned G = static_cast<unsigned>(p.head_group);
+        const unsigned per_group = G * static_cast<unsigned>(2 * T);
+        const unsigned g = blockIdx.x / per_group, rem = blockIdx.x % per_group;
+        const unsigned in_group = min(G, static_cast<unsigned>(p.B * p.H) - g * G);   // the last group may be short
+        const int y = static_cast<int>(rem / in_group);
+        const int bh = static_cast<int>(g * G + rem % in_group);
         if (y < T)
-            dkdv_cta<D>(tm, p, static_cast<int>(blockIdx.x), y);
+            dkdv_cta<D>(tm, p, bh, y);
         else
-            dq_cta<D>(tm, p, static_cast<int>(blockIdx.x), y - T);
+            dq_cta<D>(tm, p, bh, y - T);
     }
 }
 
@@ -1034,11 +1044,29 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int T = (p.N + BT - 1) / BT;
-    if (2ll * T > 65535) return cudaErrorInvalidValue;
     // launched as a programmatic dependent of bwd_pre_kernel: its CTAs set up
     // (barriers, TMEM, the first K/V or Q/dO loads) while D is still being written
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(BH), static_cast<unsigned>(atomic_dq ? T : 2 * T), 1);
+    if (atomic_dq) {
+        if (T > 65535) return cudaErrorInvalidValue;
+        cfg.gridDim = dim3(static_cast<unsigned>(BH), static_cast<unsigned>(T), 1);
+    } else {
+        const long long ctas = static_cast<long long>(BH) * 2 * T;
+        if (ctas > 0x7fffffffll) return cudaErrorInvalidValue;
+        cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+    }
+    // Groups of (b, h) units whose Q, K, V and dO fill about 32 MiB of L2 (measured: causal
+    // B1 H32 N8192 d128 backward 1522 -> 1395 us against all units interleaved; unchanged at
+    // d = 64, where a group holds 32 or more units).  The dQ-accumulating variant keeps all
+    // units interleaved (measured faster, also with head-major and grouped orders).
+    BwdParams pg = p;
+    {
+        const long long per_unit = 4ll * p.N * D * 2;
+        long long grp = (32ll << 20) / per_unit;
+        if (grp < 1) grp = 1;
+        if (grp > BH) grp = BH;
+        pg.head_group = static_cast<int>(grp);
+    }
     cfg.blockDim = dim3(kBwdThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
@@ -1049,7 +1077,7 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
     cfg.numAttrs = 1;
     if constexpr (kCanAtomic) {
         if (atomic_dq) {
-            e = cudaLaunchKernelEx(&cfg, bwd_main_kernel<D, true>, tm, p);
+            e = cudaLaunchKernelEx(&cfg, bwd_main_kernel<D, true>, tm, pg);
             if (e != cudaSuccess) return e;
             const long long n8 = rows * D / 8;
             const long long blocks = (n8 + 255) / 256;
@@ -1059,7 +1087,7 @@ cudaError_t launch_bwd_d(const BwdParams &p, cudaStream_t stream) {
             return cudaGetLastError();
         }
     }
-    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<D>, tm, p);
+    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<D>, tm, pg);
 }
 
 }  // namespace

@@ -73,6 +73,7 @@ struct BwdParams {
     float scale_log2;                 // scale * log2(e)
     unsigned *err;
     float *dq_accum;                  // nullptr, or fp32 [B, H, N, d]: dQ accumulated by the dK/dV CTAs
+    int head_group;                   // (b, h) units per group of the main grid's CTA order (set at launch)
 };
 
 cudaError_t launch_backward(const BwdParams &p, int d, cudaStream_t stream);

@@ -966,10 +966,10 @@ __device__ __forceinline__ void dq_cta(const BwdMaps &tm, const BwdParams &p, co
     if (warp == kMma) tmem_dealloc(tmem, 512);
 }
 
-// dK/dV and dQ in one grid (B*H, 2 ceil(N/128)): rows y < T of the grid are
-// dK/dV CTAs, the others dQ CTAs.  The two halves are independent (both need
-// only D), so dQ CTAs fill the SMs that the dK/dV half leaves idle in its last
-// wave instead of waiting for a second launch.
+// dK/dV and dQ in one grid of B*H*2T CTAs (T = ceil(N/128)): for each (b, h), T
+// dK/dV CTAs and T dQ CTAs.  The two kinds are independent (both need only D), so
+// dQ CTAs fill the SMs that the dK/dV CTAs leave idle in their last wave instead
+// of waiting for a second launch.
 template <int D, bool kAtomicDQ = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {

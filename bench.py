@@ -701,6 +701,16 @@ def run_profile_case(args):
         O, L = fa.fa_forward(Q, K, V)
         atomic = args.profile == "backward_atomic"
         run = lambda: fa.fa_backward(Q, K, V, O, dO, L, atomic_dq=atomic)
+    elif args.profile == "backward128":
+        # the causal d128 backward on half the heads of the headline shape (B1 H16 N8192):
+        # 168 MB of inputs (more than L2), ~0.4 GB on the device with the gradients
+        wp = workloads.WORKLOADS[PREFILL]
+        Q, K, V = workloads.prefill_inputs(wp.B, wp.H // 2, wp.N, wp.d, wp.seed, device=dev)
+        gb = torch.Generator(device=dev)
+        gb.manual_seed(wp.seed + 1000)
+        dO = torch.randn(Q.shape, generator=gb, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        O, L = fa.fa_forward(Q, K, V, causal=True)
+        run = lambda: fa.fa_backward(Q, K, V, O, dO, L, causal=True)
     else:
         wd = workloads.WORKLOADS[DECODE]
         q, Kc, Vc = workloads.decode_inputs(wd.B, wd.H, wd.N, wd.d, wd.seed, device=dev)
@@ -724,7 +734,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["prefill", "prefill64", "prefill_fp8", "decode", "backward", "backward_atomic"],
+    ap.add_argument("--profile", choices=["prefill", "prefill64", "prefill_fp8", "decode", "backward", "backward_atomic",
+                                          "backward128"],
                     default=None,
                     help="only launch one kernel warmup+steps times (for ncu captures)")
     ap.add_argument("--record-traffic", nargs=3, metavar=("REPORT", "KERNEL", "NOTE"), default=None,

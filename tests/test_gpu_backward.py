@@ -110,6 +110,20 @@ def test_backward_causal_d128_sampled_heads():
         _check(f"bwd causal h{h}", {k: v[sl] for k, v in got.items()}, ref)
 
 
+@pytest.mark.slow
+def test_backward_causal_8k_d128_bench_shape_sampled_heads():
+    """B1 H32 N8192 d128 causal (the bench's causal backward, same launch: 64 key tiles and 64
+    query tiles per head in the grouped grid); the oracle on the first and the last head,
+    every element of dQ, dK, dV (about 30 s of host time per head)."""
+    B, H, N, d = 1, 32, 8192, 128
+    Q, K, V, dO = _inputs(B, H, N, d, seed=2)
+    got = _gpu_backward(Q, K, V, dO, True)
+    for h in (0, H - 1):
+        sl = (slice(0, 1), slice(h, h + 1))
+        ref = oracle.sdpa_backward(Q[sl], K[sl], V[sl], dO[sl], causal=True, magnitudes=True)
+        _check(f"bwd causal 8k h{h}", {k: v[sl] for k, v in got.items()}, ref)
+
+
 def test_backward_is_deterministic():
     """Every gradient element is written by one CTA (no atomics): two runs agree bit for bit."""
     Q, K, V, dO = _inputs(2, 4, 1000, 64, seed=420)

@@ -37,8 +37,9 @@ PREFILL = "prefill_causal_b1h32_n8192_d128"
 DECODE = "decode_b1h32_l32768_d128"
 FLUSH_BYTES = 256 << 20
 READBACK_BYTES = 512 << 20
-L2_NOTE = ("flushed between steps, outside the timed events: a 256 MiB write, then a 512 MiB read so that "
-           "the write's dirty lines are written back before the step (inputs are never left in L2)")
+# The L2 flush between timed steps: the read writes the fill's dirty lines back before the
+# next step, so no step starts with inputs (or pending write-backs) in L2.
+L2_NOTE = "flushed between steps outside the timed events (256 MiB write, then 512 MiB read)"
 
 
 class L2Flush:
@@ -398,7 +399,7 @@ def run_ours(args, rank, world, local_rank):
         "ms": round(ms, 4), "flops": fl, "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
         "frac_of_bf16_peak": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
         "frac_of_mixed_peak": round(fl / (ms * 1e-3) / 1e12 / mixed_peak, 4),
-        "mixed_peak_tflops": round(mixed_peak, 1), "dtype": "e4m3 Q,K,V; bf16 P,V in the P V product"}
+        "mixed_peak_tflops": round(mixed_peak, 1)}
     del Q8, K8, V8, ws8, O8
     # backward (dQ, dK, dV) of the two prefill shapes; algorithmic FLOPs = 5 GEMMs of 2 d per
     # unmasked score = 2.5 x the forward's (CMU 10-423 Lecture 18, 6.1: 10 N^2 d per head)
@@ -416,8 +417,7 @@ def run_ours(args, rank, world, local_rank):
                                           workspace=wsb))
         fl = 2.5 * prefill_flops(B_, H_, N_, d_, causal_)
         others[name] = {"ms": round(ms, 4), "flops": fl, "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
-                        "frac_of_bf16_peak": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                        "kernels": "bwd_pre + bwd_main (dK/dV and dQ CTAs in one grid; S and dP recomputed in both)"}
+                        "frac_of_bf16_peak": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
         if d_ == 64:
             # fa_backward_atomic_dq: dQ accumulated by the dK/dV CTAs with TMA reductions
             # (d = 64 only); not bitwise reproducible in dQ
@@ -427,9 +427,7 @@ def run_ours(args, rank, world, local_rank):
                                               workspace=wsa, atomic_dq=True))
             others[name + "_atomic_dq"] = {
                 "ms": round(ms, 4), "flops": fl, "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
-                "frac_of_bf16_peak": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                "kernels": "memset + bwd_pre + bwd_main (dK/dV CTAs also form dQ partials, added into an fp32 "
-                           "copy by TMA reductions) + dq_finalize"}
+                "frac_of_bf16_peak": round(fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
             del wsa
         del Qb, Kb, Vb, dOb, Ob, Lb, dQb, dKb, dVb
     st, site = fa.fa_device_error(clear=True)
@@ -495,8 +493,7 @@ def run_ours(args, rank, world, local_rank):
                      "kernel": "prefill_kernel<128>"},
         "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(ee, 4), "step_ms": spread(e2e_ms),
-                "path": "fa_forward_host: pinned host Q,K,V -> device by groups of heads, each group's "
-                        "forward and O, L copy back overlapping the next groups' copies"},
+                "path": "fa_forward_host: pinned host buffers, copies inside the call, pipelined by head groups"},
         "decode": {"workload": DECODE, "value": round(gbs, 1), "unit": "GB/s",
                    "ms_per_step": round(dc, 4), "step_ms": spread(dc_ms), "bytes_per_step": dbytes,
                    "num_splits": "auto",
@@ -608,6 +605,29 @@ def oracle_extras(threads):
         tiny[key] = (time.perf_counter() - t0) * 1e3
     tiny["tflops_1_thread"] = flops / (tiny["ms_1_thread"] * 1e-3) / 1e12
     out["tiny"] = tiny
+    return out
+
+
+# Key order of the printed line: the contract's keys first, the per-workload detail last.
+LINE_ORDER = ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks",
+              "cpu_baseline", "step_ms", "wall_s_timed_region", "decode", "other_workloads")
+
+
+def rounded(x, digits=4):
+    """Floats in nested dicts to `digits` significant digits (integers and strings unchanged)."""
+    if isinstance(x, float):
+        return float(f"{x:.{digits}g}")
+    if isinstance(x, dict):
+        return {k: rounded(v, digits) for k, v in x.items()}
+    return x
+
+
+def ordered_line(res):
+    out = {k: res[k] for k in LINE_ORDER if k in res}
+    out.update({k: v for k, v in res.items() if k not in out})
+    if "cpu_baseline" in out:
+        out["cpu_baseline"] = rounded(out["cpu_baseline"])
     return out
 
 
@@ -755,7 +775,7 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args)), flush=True)
+            print(json.dumps(ordered_line(run_reference(args))), flush=True)
         return
 
     if world > 1:
@@ -769,7 +789,7 @@ def main():
             v, threads, desc = oracle_sample(args.cpu_seconds)
             res["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                    "sample": desc, **oracle_extras(threads)}
-        print(json.dumps(res), flush=True)
+        print(json.dumps(ordered_line(res)), flush=True)
     if world > 1:
         import torch
         torch.distributed.barrier()
